@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Throughput of the EXL3 trellis tile encoder (one JSON line on stdout).
+
+A step is one pass of the whole path -- rotate, rms, scale, trellis encode,
+decode, inverse rotation, MSE (exl3_quantize at g = 1) -- over one synthetic
+4096x4096 bf16 weight (65,536 tiles of 16x16, K = 2).  Inputs are resident in
+device memory before timing; the L2 cache is flushed (256 MiB write) between
+steps, outside the per-step CUDA events.  The dominant kernel (the trellis
+encoder) is timed live with CUDA events the library records around each of its
+launches during the timed steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank quantizes its own copy of the workload (weak scaling,
+no collective on the data path); the reported time is the maximum over ranks.
+--impl reference times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "16x16 tiles/sec encoded at K=2/4 on 1 GB300; % of INT32/FP32 ALU roofline"
+UNIT = "tiles/s"
+
+# Algorithmic lane-operations per tile (two passes of 256 steps): per step
+# 2^16 * 3 (sub, mul, add) + 2^(16-K) * (2^K - 1) * 2 (compare, select).
+def alg_ops_per_tile(K: int) -> float:
+    return 2 * 256 * (65536 * 3 + (1 << (16 - K)) * ((1 << K) - 1) * 2)
+
+
+# GB300: 152 SMs, 128 lanes issue per SM per clock, 2070 MHz maximum SM clock.
+ALU_LANES_PER_SM_CLK = 128
+SM_MAX_MHZ_NOMINAL = 2070.0
+
+# DRAM traffic of one encode launch per tile, from an ncu capture
+# (profiles/encode_k2_linear4096.md); valid only for the source it was taken on.
+ENCODE_TRAFFIC = {
+    # "sha256 of csrc/encode.cu": bytes per tile
+}
+
+WORKLOAD = "linear4096_k2"
+WORKLOAD_DESC = ("one 4096x4096 bf16 linear weight, N(0, 0.02^2) plus 0.1% outliers x8, "
+                 "random +-1 su/sv, randomized Hadamard rotation, K=2, scale = rms(R) (g=1)")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
+
+
+def _src_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxs.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_setup(n_sample: int, seed: int = 0):
+    """Rotated targets of the workload and a seeded sample of tile indices."""
+    import numpy as np
+    import oracle
+    from exl3_trellis_weight_gb300 import inputs
+    (_, W, su, sv, K), = inputs.workload(WORKLOAD)
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    _, inv = oracle.scale_for(1.0, oracle.rms(R))
+    n = (R.shape[0] // 16) * (R.shape[1] // 16)
+    idx = np.random.default_rng(seed).choice(n, n_sample, replace=False)
+    return R, K, inv, idx
+
+
+def oracle_time(R, K, inv, idx, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.encode_matrix(R, K, inv, tiles=idx, threads=threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    per_step = max(threads * 2, 32)
+    R, K, inv, idx_all = oracle_sample_setup(per_step * (args.warmup + args.steps), seed=123)
+    times = []
+    for s in range(args.warmup + args.steps):
+        idx = idx_all[s * per_step:(s + 1) * per_step]
+        dt = oracle_time(R, K, inv, idx, threads)
+        if s >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = per_step * args.steps / tot
+    sample = (f"{per_step} seeded random tiles per step of the rotated {WORKLOAD} matrix "
+              f"(rotation and rms done once before timing); trellis encode of each tile")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "description": WORKLOAD_DESC, "K": K,
+                   "tiles_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import exl3_trellis_weight_gb300 as ex
+    from exl3_trellis_weight_gb300 import inputs
+
+    (_, W_cpu, su_cpu, sv_cpu, K), = inputs.workload(WORKLOAD)
+    rows, cols = W_cpu.shape
+    n_tiles = (rows // 16) * (cols // 16)
+    W = W_cpu.to(dev)
+    su, sv = su_cpu.to(dev), sv_cpu.to(dev)
+    codes = torch.empty(rows // 16, cols // 16, 16 * K, dtype=torch.int16, device=dev)
+    ws = torch.empty(ex.quantize_workspace_bytes(rows, cols, K), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return ex.quantize(W, su, sv, K, 1.0, codes=codes, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ex.profile_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        res = step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    enc_ms, enc_n, launches = ex.profile_read()
+    ex.profile_enable(False)
+    barrier(world, dev)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    tot_s = sum(step_ms) / 1e3
+    tot_s_max = max_over_ranks(tot_s, world, dev)
+    value = n_tiles * args.steps * world / tot_s_max
+    mse_val = float(res["mse"].item())
+
+    # ---- roofline of the dominant kernel (encode) ----------------------------
+    peaks, peak_kind = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    f_max = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL))
+    peak_tops = sms * ALU_LANES_PER_SM_CLK * f_max * 1e6 / 1e12
+    enc_launch_s = (enc_ms / max(enc_n, 1)) / 1e3
+    ops_launch = alg_ops_per_tile(K) * n_tiles
+    achieved = ops_launch / enc_launch_s / 1e12
+    sha = _src_sha(os.path.join(ROOT, "exl3_trellis_weight_gb300", "csrc", "encode.cu"))
+    tpt = ENCODE_TRAFFIC.get(sha)
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Tops/s",
+                "frac": achieved / peak_tops,
+                "traffic": (tpt * n_tiles) if tpt is not None else None,
+                "kernel": "encode_kernel<2>",
+                "peak_basis": f"{sms} SMs x {ALU_LANES_PER_SM_CLK} lane-ops/clk x {f_max:.0f} MHz "
+                              f"(max SM clock, {peak_kind})",
+                "alg_ops_per_tile": alg_ops_per_tile(K),
+                "encode_ms_per_launch": enc_launch_s * 1e3,
+                "encode_share_of_step": (enc_ms / 1e3) / tot_s}
+    if clk:
+        roofline["frac_at_sampled_clock"] = achieved / (sms * ALU_LANES_PER_SM_CLK * clk["sm_mhz"] * 1e6 / 1e12)
+
+    # ---- rotation kernel HBM throughput -------------------------------------------
+    R = torch.empty(rows, cols, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ex.rotate(W, su, sv, out=R)
+    rot_ms = []
+    for _ in range(10):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ex.rotate(W, su, sv, out=R)
+        b.record(stream)
+        b.synchronize()
+        rot_ms.append(a.elapsed_time(b))
+    rot_bytes = rows * cols * (2 + 4)
+    rot_gbs = rot_bytes / (statistics.median(rot_ms) / 1e3) / 1e9
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    rotation = {"bound": "hbm", "achieved": rot_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": rot_gbs / hbm_peak, "bytes_per_launch": rot_bytes,
+                "ms_per_launch": statistics.median(rot_ms)}
+
+    # ---- end to end through host buffers ----------------------------------------
+    W_h = W_cpu.pin_memory()
+    su_h, sv_h = su_cpu.pin_memory(), sv_cpu.pin_memory()
+    codes_h = torch.empty(codes.shape, dtype=torch.int16).pin_memory()
+    scal_h = torch.empty(2, dtype=torch.float64).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        W.copy_(W_h, non_blocking=True)
+        su.copy_(su_h, non_blocking=True)
+        sv.copy_(sv_h, non_blocking=True)
+        r = ex.quantize(W, su, sv, K, 1.0, codes=codes, ws=ws)
+        codes_h.copy_(codes, non_blocking=True)
+        scal_h[0:1].copy_(r["mse"].reshape(1), non_blocking=True)
+        scal_h[1:2].copy_(r["scale"].double().reshape(1), non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world, dev)
+    h2d = W_h.numel() * 2 + (su_h.numel() + sv_h.numel()) * 4
+    d2h = codes_h.numel() * 2 + 8 + 4
+    e2e = {"value": n_tiles * args.steps * world / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---- K=4 line: 12288x4096 Student-t weight ---------------------------------------
+    k4 = None
+    if not args.skip_k4:
+        (_, W4c, su4c, sv4c, K4), = inputs.workload("mlp12288_t5_k4")
+        W4, su4, sv4 = W4c.to(dev), su4c.to(dev), sv4c.to(dev)
+        r4, c4 = W4.shape
+        nt4 = (r4 // 16) * (c4 // 16)
+        ws4 = torch.empty(ex.quantize_workspace_bytes(r4, c4, K4), dtype=torch.uint8, device=dev)
+        codes4 = torch.empty(r4 // 16, c4 // 16, 16 * K4, dtype=torch.int16, device=dev)
+        ex.quantize(W4, su4, sv4, K4, 1.0, codes=codes4, ws=ws4)
+        torch.cuda.synchronize(dev)
+        ex.profile_enable(True)
+        k4_ms = []
+        for _ in range(2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.quantize(W4, su4, sv4, K4, 1.0, codes=codes4, ws=ws4)
+            b.record(stream)
+            b.synchronize()
+            k4_ms.append(a.elapsed_time(b))
+        e4_ms, e4_n, _ = ex.profile_read()
+        ex.profile_enable(False)
+        ach4 = alg_ops_per_tile(K4) * nt4 / ((e4_ms / max(e4_n, 1)) / 1e3) / 1e12
+        k4 = {"workload": "mlp12288_t5_k4: 12288x4096 bf16 Student-t(5) std 0.015, K=4",
+              "tiles": nt4, "tiles_per_s": nt4 * len(k4_ms) / (sum(k4_ms) / 1e3),
+              "encode_tiles_per_s": nt4 / ((e4_ms / max(e4_n, 1)) / 1e3),
+              "roofline_frac": ach4 / peak_tops, "achieved_tops": ach4}
+        del W4, ws4, codes4
+
+    # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        import oracle
+        oracle.build()
+        threads = oracle.default_threads()
+        n_s = max(8 * threads, 64)
+        Rn, Kc, inv, idx = oracle_sample_setup(n_s, seed=7)
+        dt = oracle_time(Rn, Kc, inv, idx, threads)
+        cpu = {"value": n_s / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n_s} seeded random tiles of the rotated {WORKLOAD} matrix, trellis "
+                         f"encode only (rotation/rms done once before timing), {dt:.1f} s wall"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_s_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "description": WORKLOAD_DESC, "K": K,
+                       "tiles": n_tiles, "rows": rows, "cols": cols,
+                       "l2": "flushed between steps (256 MiB write, outside the step events)",
+                       "step": "exl3_quantize: rotate, rms, scale, encode, decode, inverse rotate, MSE"},
+            "weights_per_s": value * 256,
+            "mse": mse_val,
+            "roofline": roofline,
+            "rotation": rotation,
+            "k4": k4,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-k4", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

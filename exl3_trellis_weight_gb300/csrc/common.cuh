@@ -1,0 +1,154 @@
+// common.cuh -- shared definitions for the libexl3 CUDA kernels (sm_103a).
+//
+// Everything on the encode/decode/rotation path is IEEE binary32 with
+// round-to-nearest and no contraction: the library is compiled with
+// -fmad=false and the hot arithmetic uses the explicit __f*_rn intrinsics.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/exl3.h"
+
+namespace exl3 {
+
+// ---------------------------------------------------------------------------
+// mul1 codebook (page "EXL3 Intel Arc Quantizer", Core Implemented
+// Architecture item 5: a procedural codebook with fp16 levels).  The
+// multiplier and scale are this library's reading of that passage:
+//   v(s) = fp16_rn( fl32( (bytesum(u32(s * 0x9E3779B1)) - 510) * c ) ),
+//   c = fl32(1 / 147.9146802...), the inverse population standard deviation
+//   of that byte sum over the 65536 states.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMul1Mult = 0x9E3779B1u;
+constexpr float kMul1C = 0x1.bb10f4p-8f;
+
+__host__ __device__ __forceinline__ int mul1_bytesum(uint32_t state) {
+    uint32_t x = state * kMul1Mult;
+    return (int)(x & 0xFFu) + (int)((x >> 8) & 0xFFu) + (int)((x >> 16) & 0xFFu) +
+           (int)(x >> 24);
+}
+
+__device__ __forceinline__ __half mul1_half(uint32_t state) {
+    float f = __fmul_rn((float)(mul1_bytesum(state) - 510), kMul1C);
+    return __float2half_rn(f);
+}
+
+__device__ __forceinline__ float mul1_value(uint32_t state) {
+    return __half2float(mul1_half(state));
+}
+
+// ---------------------------------------------------------------------------
+// Trellis geometry for K bits per step on the 16-bit bitshift trellis.
+//   tracked row:   G = 2^(16-K) entries, index g = low 16-K bits of a state
+//   candidates:    sigma_k = (k << (16-K)) | g,  k in [0, 2^K)
+//   predecessor:   sigma_k >> K = (k << (16-2K)) | (g >> K)
+// A "unit" h' = g >> K groups the 2^K tracked entries g = (h' << K) | j that
+// read the same 2^K predecessor costs M((k << (16-2K)) | h').  Each of the
+// 1024 threads of an encode block owns 64 candidate states:
+//   K=2: 4 units x 4 groups x 4 candidates   (units h' = u*1024 + tid)
+//   K=3: 1 unit  x 8 groups x 8 candidates   (unit h' = tid)
+//   K=4: 1/4 unit: 4 groups x 16 candidates  (unit h' = tid >> 2,
+//                                             groups 4*(tid & 3) .. +3)
+// ---------------------------------------------------------------------------
+constexpr int kThreads = 1024;
+
+template <int K>
+struct Geo {
+    static constexpr int KR = 16 - K;
+    static constexpr int NK = 1 << K;
+    static constexpr int G = 1 << KR;
+    static constexpr int UNITS = 1 << (16 - 2 * K);
+    static constexpr int NU = UNITS >= kThreads ? UNITS / kThreads : 1;  // units per thread
+    static constexpr int TPU = UNITS >= kThreads ? 1 : kThreads / UNITS; // threads per unit
+    static constexpr int NJ = NK / TPU;                                  // groups per thread-unit
+    static constexpr int STATES = NU * NJ * NK;                          // = 64
+    static_assert(STATES == 64, "each thread owns 64 candidate states");
+    static_assert(NU * NJ * K <= 32, "decisions of one thread fit a 32-bit word");
+
+    __device__ __forceinline__ static int unit(int u, int tid) {
+        return TPU == 1 ? u * kThreads + tid : (tid / TPU);
+    }
+    __device__ __forceinline__ static int j0(int tid) {
+        return TPU == 1 ? 0 : (tid % TPU) * NJ;
+    }
+    // Location of D_t(g) inside a decision row: (word index, bit position).
+    __host__ __device__ __forceinline__ static void dec_locate(uint32_t g, int &word, int &bit) {
+        uint32_t hp = g >> K;
+        uint32_t j = g & (NK - 1);
+        if (TPU == 1) {
+            word = (int)(hp & (kThreads - 1));
+            int u = (int)(hp / kThreads);
+            bit = (u * NJ + (int)j) * K;
+        } else {
+            word = (int)(hp * TPU + j / NJ);
+            bit = (int)(j % NJ) * K;
+        }
+    }
+};
+
+// Decision rows: one 32-bit word per thread per step (4 KiB per row).
+constexpr int kRowWords = kThreads;
+constexpr int kRowsPass1 = 128;   // steps 127..254 of the rolled pass
+constexpr int kRowsPass2 = 255;   // steps 0..254 of the constrained pass
+constexpr size_t kEncodeBlockScratchBytes =
+    (size_t)2 * (kRowsPass1 + kRowsPass2) * kRowWords * sizeof(uint32_t);
+
+// ---------------------------------------------------------------------------
+// host-side helpers
+// ---------------------------------------------------------------------------
+exl3_status set_error(exl3_status st, const char *fmt, ...);
+exl3_status cuda_check(cudaError_t e, const char *what);
+int device_sm_count();
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// launch accounting for exl3_profile_* (abi.cu)
+void note_launch();
+void profile_encode_begin(cudaStream_t s);
+void profile_encode_end(cudaStream_t s);
+
+// internal launchers (no argument checks; the ABI layer checks)
+struct EncodeLaunch {
+    const float *Y;
+    int64_t rows, cols;
+    int K;
+    float inv_scale;             // used when inv_scale_dev == nullptr
+    const float *inv_scale_dev;  // device scalar or nullptr
+    uint32_t *codes;             // [n_tiles][8K] uint32
+    float *tile_cost;            // nullable
+    uint32_t *scratch;           // grid * kEncodeBlockScratchBytes
+    int grid;
+};
+exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s);
+
+exl3_status launch_decode(const uint32_t *codes, int64_t rows, int64_t cols, int K,
+                          float scale, const float *scale_dev, float *out, cudaStream_t s);
+
+// rotation modes
+enum RotSrc { SRC_F32 = 0, SRC_BF16 = 1, SRC_CODES = 2 };
+struct RotateLaunch {
+    int inverse;
+    int src;                  // RotSrc
+    const void *in;           // fp32/bf16 matrix or uint32 codes
+    int K;                    // SRC_CODES only
+    const float *scale_dev;   // SRC_CODES only: decode scale (device)
+    const float *su, *sv;
+    int64_t rows, cols;
+    float *out;               // nullable: skip the store
+    const void *ref;          // nullable: per-tile fp64 sum of (ref - out)^2
+    int ref_dt;
+    double *tile_sums;        // per-tile sums: of out^2 (ref == null) or of (ref-out)^2
+};
+exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s);
+
+exl3_status launch_tile_sumsq(const void *x, int x_dt, const float *ref, int64_t rows,
+                              int64_t cols, double *tile_sums, cudaStream_t s);
+// tree sum of n doubles; scratch >= tree_scratch_doubles(n) doubles; result -> *out
+size_t tree_scratch_doubles(int64_t n);
+exl3_status launch_tree_sum(const double *in, int64_t n, double *scratch, double *out,
+                            cudaStream_t s);
+
+}  // namespace exl3

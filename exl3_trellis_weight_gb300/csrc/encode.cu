@@ -1,0 +1,351 @@
+// encode.cu -- persistent trellis tile encoder (page "EXL3 Intel Arc
+// Quantizer", Core Implemented Architecture items 1, 4 and 5).
+//
+// One 1024-thread block per SM walks its share of the tiles.  For each tile:
+//   pass 1: targets rolled left by 128, free start, 256 add-compare-select
+//           steps; decisions of steps 127..254 are kept; the lowest-index
+//           minimal final state is traced back to step 127 -> end_state.
+//   pass 2: unrolled targets, first predecessor fixed to end_state, 255 steps
+//           (step 255 of the constrained pass is never needed: its path is
+//           forced to end at end_state); traced back from end_state; the low
+//           K bits of each state are packed MSB first.
+//
+// The tracked cost row M (2^(16-K) fp32) is double-buffered in shared memory;
+// the mul1 level of each of a thread's 64 candidate states is fixed for the
+// whole launch and is kept in registers as packed fp16.  Decisions (K bits per
+// tracked entry per step, one 32-bit word per thread per step) go to the
+// block's slice of the workspace.
+//
+// The traceback is a chain of dependent loads, so it is overlapped with the
+// forward pass of another tile: the block keeps two tiles A and B in flight
+// and cycles through four phases
+//     fwd1(A) | tb2(prev B);  fwd1(B) | tb1(A);  fwd2(A) | tb1(B);  fwd2(B) | tb2(A)
+// where thread 0 performs one traceback step per forward step, issuing the
+// load at the start of the step and consuming it at the end.
+#include "common.cuh"
+
+namespace exl3 {
+
+namespace {
+
+__device__ __forceinline__ float half_at(const uint32_t (&vpk)[32], int idx) {
+    const uint32_t w = vpk[idx >> 1];
+    const unsigned short h = (idx & 1) ? (unsigned short)(w >> 16) : (unsigned short)(w & 0xFFFFu);
+    return __half2float(__ushort_as_half(h));
+}
+
+template <int K>
+__device__ __forceinline__ void put_code(uint32_t *bs, int t, uint32_t e) {
+    const int p = t * K;
+    const int w = p >> 5;
+    const int sh = 32 - K - (p & 31);
+    if (sh >= 0) {
+        bs[w] |= e << sh;
+    } else {
+        bs[w] |= e >> (-sh);
+        bs[w + 1] |= e << (32 + sh);
+    }
+}
+
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w < v ? w : v;
+    }
+    return v;
+}
+
+// One add-compare-select step over the thread's 64 candidate states.
+//   M_t(g) = min_k fl(M_{t-1}((k << (16-2K)) | (g >> K)) + fl(fl(y - v)^2)),
+// lowest k on ties.  Writes the thread's decision word; with ARGMIN, instead
+// of storing M_t it folds (cost, full state index) of each tracked entry into
+// `key` (lexicographic minimum).
+template <int K, bool ARGMIN>
+__device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__restrict__ Mn,
+                                         const float y, const uint32_t (&vpk)[32], const int tid,
+                                         uint32_t &word, unsigned long long &key) {
+    using Gm = Geo<K>;
+    word = 0u;
+#pragma unroll
+    for (int u = 0; u < Gm::NU; u++) {
+        const int hp = Gm::unit(u, tid);
+        const int j0 = Gm::j0(tid);
+        float m[Gm::NK];
+#pragma unroll
+        for (int k = 0; k < Gm::NK; k++)
+            m[k] = Mp[(k << (16 - 2 * K)) | hp];
+        float outv[Gm::NJ];
+#pragma unroll
+        for (int jj = 0; jj < Gm::NJ; jj++) {
+            float best = 0.0f;
+            uint32_t bk = 0u;
+#pragma unroll
+            for (int k = 0; k < Gm::NK; k++) {
+                const float v = half_at(vpk, (u * Gm::NK + k) * Gm::NJ + jj);
+                const float d = __fsub_rn(y, v);
+                const float c = __fadd_rn(m[k], __fmul_rn(d, d));
+                if (k == 0) {
+                    best = c;
+                } else if (c < best) {
+                    best = c;
+                    bk = (uint32_t)k;
+                }
+            }
+            outv[jj] = best;
+            word |= bk << ((u * Gm::NJ + jj) * K);
+            if (ARGMIN) {
+                const uint32_t g = ((uint32_t)hp << K) | (uint32_t)(j0 + jj);
+                const uint32_t full = (bk << Gm::KR) | g;
+                const unsigned long long kk =
+                    ((unsigned long long)__float_as_uint(best) << 32) | full;
+                key = kk < key ? kk : key;
+            }
+        }
+        if (!ARGMIN) {
+            float *dst = Mn + (((uint32_t)hp << K) | (uint32_t)j0);
+            if (Gm::NJ == 2) {
+                *reinterpret_cast<float2 *>(dst) = make_float2(outv[0], outv[1 % Gm::NJ]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < Gm::NJ; q += 4)
+                    *reinterpret_cast<float4 *>(dst + q) =
+                        make_float4(outv[q], outv[(q + 1) % Gm::NJ], outv[(q + 2) % Gm::NJ],
+                                    outv[(q + 3) % Gm::NJ]);
+            }
+        }
+    }
+}
+
+struct Tb {          // traceback state, kept in shared memory, used by thread 0 only
+    const uint32_t *rows;
+    int tile;
+    uint32_t s;       // full state at step t
+    uint32_t pending; // decision word in flight
+    int t, stop, row0, pass, slot;
+    bool on;
+};
+
+template <int K>
+__device__ __forceinline__ void tb_issue(Tb &tb) {
+    int w, b;
+    Geo<K>::dec_locate(tb.s >> K, w, b);
+    tb.pending = __ldcg(tb.rows + (size_t)(tb.t - 1 - tb.row0) * kRowWords + w);
+}
+
+template <int K>
+__device__ __forceinline__ void tb_advance(Tb &tb, uint32_t *bs) {
+    using Gm = Geo<K>;
+    const uint32_t g = tb.s >> K;
+    int w, b;
+    Gm::dec_locate(g, w, b);
+    const uint32_t k = (tb.pending >> b) & (uint32_t)(Gm::NK - 1);
+    tb.s = (k << Gm::KR) | g;
+    tb.t -= 1;
+    if (tb.pass == 2)
+        put_code<K>(bs, tb.t, tb.s & (uint32_t)(Gm::NK - 1));
+    if (tb.t == tb.stop)
+        tb.on = false;
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch a) {
+    using Gm = Geo<K>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *M0 = reinterpret_cast<float *>(smem);
+    float *M1 = M0 + Gm::G;
+    float *ys = M1 + Gm::G;                                       // 256 targets
+    uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);         // packed codes (tb2)
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
+    __shared__ uint32_t sh_sstar[2], sh_end[2];
+    __shared__ Tb tb;
+
+    const int tid = threadIdx.x;
+
+    // mul1 levels of this thread's candidate states, packed two per register
+    uint32_t vpk[32];
+#pragma unroll
+    for (int u = 0; u < Gm::NU; u++)
+#pragma unroll
+        for (int k = 0; k < Gm::NK; k++)
+#pragma unroll
+            for (int jj = 0; jj < Gm::NJ; jj += 2) {
+                const uint32_t g = ((uint32_t)Gm::unit(u, tid) << K) | (uint32_t)(Gm::j0(tid) + jj);
+                const uint32_t s0 = ((uint32_t)k << Gm::KR) | g;
+                const unsigned short h0 = __half_as_ushort(mul1_half(s0));
+                const unsigned short h1 = __half_as_ushort(mul1_half(s0 + 1u));
+                vpk[((u * Gm::NK + k) * Gm::NJ + jj) >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            }
+
+    const float inv_s = a.inv_scale_dev ? __ldg(a.inv_scale_dev) : a.inv_scale;
+    // tile bookkeeping fits 32 bits: the ABI bounds a matrix to 2^34 elements
+    const int tiles_c = (int)(a.cols / 16);
+    const int n_tiles = (int)(a.rows / 16) * tiles_c;
+    const int grid = (int)gridDim.x;
+    const int n_my = n_tiles > (int)blockIdx.x ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
+    // decision buffers of this block: pass-1 slots 0/1, then pass-2 slots 0/1
+    uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
+    constexpr size_t kP1 = (size_t)kRowsPass1 * kRowWords, kP2 = (size_t)kRowsPass2 * kRowWords;
+
+    if (tid == 0) {
+        tb.on = false;
+        tb.rows = nullptr;
+        tb.tile = 0;
+        tb.s = tb.pending = 0u;
+        tb.t = tb.stop = tb.row0 = tb.pass = tb.slot = 0;
+    }
+
+    const int npairs = (n_my + 1) / 2;
+    for (int ph = 0; ph <= npairs * 4; ph++) {
+        const int p = ph >> 2;
+        const int sub = ph & 3;
+        int f_slot = 0, f_pass = 0, b_slot = 0, b_pass = 0;
+        int f_loc = -1, b_loc = -1;
+        if (p < npairs) {
+            const int A = 2 * p, B = 2 * p + 1;
+            const bool hasB = B < n_my;
+            if (sub == 0) {
+                f_slot = 0; f_pass = 1; f_loc = A;
+                if (p > 0) { b_slot = 1; b_pass = 2; b_loc = 2 * p - 1; }
+            } else if (sub == 1) {
+                if (hasB) { f_slot = 1; f_pass = 1; f_loc = B; }
+                b_slot = 0; b_pass = 1; b_loc = A;
+            } else if (sub == 2) {
+                f_slot = 0; f_pass = 2; f_loc = A;
+                if (hasB) { b_slot = 1; b_pass = 1; b_loc = B; }
+            } else {
+                if (hasB) { f_slot = 1; f_pass = 2; f_loc = B; }
+                b_slot = 0; b_pass = 2; b_loc = A;
+            }
+        } else if (p > 0 && 2 * p - 1 < n_my) {
+            b_slot = 1; b_pass = 2; b_loc = 2 * p - 1;   // drain: last B's traceback
+        }
+        const bool fwd = f_loc >= 0;
+        const int f_tile = (int)blockIdx.x + f_loc * grid;
+
+        if (fwd) {
+            const int tr = f_tile / tiles_c, tc = f_tile % tiles_c;
+            if (tid < 256) {
+                const int i = (f_pass == 1) ? ((tid + 128) & 255) : tid;
+                const float *src = a.Y + (size_t)(tr * 16 + (i >> 4)) * (size_t)a.cols + tc * 16 + (i & 15);
+                ys[tid] = __fmul_rn(__ldg(src), inv_s);
+            }
+            if (f_pass == 1) {
+                for (int g = tid; g < Gm::G; g += kThreads)
+                    M0[g] = 0.0f;
+            } else {
+                const int ge = (int)(sh_end[f_slot] & (uint32_t)(Gm::G - 1));
+                for (int g = tid; g < Gm::G; g += kThreads)
+                    M0[g] = (g == ge) ? 0.0f : __int_as_float(0x7f800000);
+            }
+        }
+        if (tid == 0 && b_loc >= 0) {
+            tb.on = true;
+            tb.pass = b_pass;
+            tb.slot = b_slot;
+            tb.tile = (int)blockIdx.x + b_loc * grid;
+            tb.t = 255;
+            if (b_pass == 1) {
+                tb.s = sh_sstar[b_slot];
+                tb.stop = 127;
+                tb.rows = scr + (size_t)b_slot * kP1;
+                tb.row0 = 127;
+            } else {
+                tb.s = sh_end[b_slot];
+                tb.stop = 0;
+                tb.rows = scr + 2 * kP1 + (size_t)b_slot * kP2;
+                tb.row0 = 0;
+                for (int w = 0; w < 8 * K; w++)
+                    bs[w] = 0u;
+                put_code<K>(bs, 255, tb.s & (uint32_t)(Gm::NK - 1));
+            }
+        }
+        __syncthreads();
+
+        if (fwd) {
+            uint32_t *rows = (f_pass == 1) ? scr + (size_t)f_slot * kP1
+                                           : scr + 2 * kP1 + (size_t)f_slot * kP2;
+            const int row0 = (f_pass == 1) ? 127 : 0;
+            for (int t = 0; t < 255; t++) {
+                if (tid == 0 && tb.on)
+                    tb_issue<K>(tb);
+                const float *Mp = (t & 1) ? M1 : M0;
+                float *Mn = (t & 1) ? M0 : M1;
+                uint32_t word;
+                unsigned long long key = 0ull;
+                acs_step<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
+                if (t >= row0)
+                    rows[(size_t)(t - row0) * kRowWords + tid] = word;
+                if (tid == 0 && tb.on)
+                    tb_advance<K>(tb, bs);
+                __syncthreads();
+            }
+            if (f_pass == 1) {
+                // step 255 (reads M_254 from M1): lowest full state with minimal cost
+                if (tid == 0 && tb.on)
+                    tb_issue<K>(tb);
+                uint32_t word;
+                unsigned long long key = ~0ull;
+                acs_step<K, true>(M1, nullptr, ys[255], vpk, tid, word, key);
+                if (tid == 0 && tb.on)
+                    tb_advance<K>(tb, bs);
+                key = warp_min_u64(key);
+                if ((tid & 31) == 0)
+                    red[tid >> 5] = key;
+                __syncthreads();
+                if (tid < 32) {
+                    key = warp_min_u64(red[tid]);
+                    if (tid == 0)
+                        sh_sstar[f_slot] = (uint32_t)(key & 0xffffffffull);
+                }
+            } else if (tid == 0 && a.tile_cost) {
+                // path forced to end at end_state: fl(M_254(end >> K) + q_255(end))
+                const uint32_t e = sh_end[f_slot];
+                const float d = __fsub_rn(ys[255], mul1_value(e));
+                a.tile_cost[f_tile] = __fadd_rn(M1[e >> K], __fmul_rn(d, d));
+            }
+        }
+        if (tid == 0 && b_loc >= 0) {
+            while (tb.on) {
+                tb_issue<K>(tb);
+                tb_advance<K>(tb, bs);
+            }
+            if (tb.pass == 1) {
+                sh_end[tb.slot] = tb.s;
+            } else {
+                uint32_t *dst = a.codes + (size_t)tb.tile * (8 * K);
+                for (int w = 0; w < 8 * K; w++)
+                    dst[w] = bs[w];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int K>
+exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s) {
+    using Gm = Geo<K>;
+    const size_t smem = (size_t)(2 * Gm::G + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(encode_kernel<K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaFuncSetAttribute(encode)");
+    profile_encode_begin(s);
+    encode_kernel<K><<<p.grid, kThreads, smem, s>>>(p);
+    note_launch();
+    profile_encode_end(s);
+    return cuda_check(cudaGetLastError(), "encode launch");
+}
+
+}  // namespace
+
+exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s) {
+    switch (p.K) {
+    case 2: return launch_k<2>(p, s);
+    case 3: return launch_k<3>(p, s);
+    case 4: return launch_k<4>(p, s);
+    default: return set_error(EXL3_ERR_UNSUPPORTED, "K=%d is not built", p.K);
+    }
+}
+
+}  // namespace exl3

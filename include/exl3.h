@@ -1,0 +1,217 @@
+/*
+ * exl3.h -- C ABI of libexl3: the EXL3 trellis tile encoder on GB300 (sm_103a).
+ *
+ * Pipeline (page "EXL3 Intel Arc Quantizer", section "Core Implemented
+ * Architecture", items 1, 4, 5, 7, 10; page "alpha2beta/JEV-9B-EXL3-K2",
+ * section 2):
+ *   W --exl3_rotate--> R = 2^-7 H (su.W.sv) H      (blockwise 128x128)
+ *     --exl3_encode_tiles(scale s)--> packed K-bit codes per 16x16 tile
+ *     --exl3_decode_tiles--> Yhat = v(state) * s
+ *     --exl3_rotate(inverse)--> What;  MSE(W, What)
+ *   exl3_quantize runs the whole chain at one relative scale g (s = g * rms(R));
+ *   exl3_gss_scale runs it inside a golden-section search over g.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     the library never frees or retains them after the call returns.
+ *   - Matrices are dense row-major with no padding: element (r, c) at r*cols+c.
+ *   - Tiles are 16x16; tile (tr, tc) has index tr*(cols/16)+tc and its 256
+ *     elements are taken row-major.  Codes are uint16 [rows/16][cols/16][16*K]
+ *     (see exl3_encode_tiles for the bit layout).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
+ *     is enqueued on it; no entry point synchronises the host with the device.
+ *   - The library allocates no device memory.  Scratch comes from the caller's
+ *     workspace `ws` (device, 256-byte aligned) of `ws_bytes` bytes, sized with
+ *     the matching *_workspace_bytes query.  The workspace must not be used by
+ *     anything else until the enqueued work has finished.
+ *   - Every argument is checked before anything is enqueued; on a non-OK
+ *     status nothing was enqueued (except EXL3_ERR_CUDA, which reports a
+ *     failed launch) and no output is promised.  exl3_last_error() returns a
+ *     message for the calling thread's last failure.
+ *   - Inputs must be finite.  Non-finite inputs produce unspecified codes and
+ *     values but never an out-of-bounds access: every data-dependent index in
+ *     the kernels is masked to its table.
+ *   - Arithmetic: IEEE binary32 with round-to-nearest and no FMA contraction
+ *     on the encode/decode/rotation path; binary64 for reductions and the
+ *     search.  Results are bit-for-bit reproducible run to run.
+ */
+#ifndef EXL3_H
+#define EXL3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EXL3_API __attribute__((visibility("default")))
+#else
+#define EXL3_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EXL3_OK = 0,
+    EXL3_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad bracket */
+    EXL3_ERR_UNSUPPORTED = 2,  /* K outside the built set, dims not multiples of 16/128 */
+    EXL3_ERR_WORKSPACE = 3,    /* ws_bytes below the minimum for this call */
+    EXL3_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+} exl3_status;
+
+typedef enum { EXL3_F32 = 0, EXL3_BF16 = 1 } exl3_dtype;
+
+/* Static string for a status code (never NULL). */
+EXL3_API const char *exl3_status_str(int status);
+
+/* Message for the calling thread's most recent non-OK status (never NULL). */
+EXL3_API const char *exl3_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+EXL3_API int exl3_version(void);
+
+/* 1 if this build encodes at K bits per weight, else 0.  K in {2, 3, 4}. */
+EXL3_API int exl3_supports_k(int K);
+
+/*
+ * Blockwise randomized Hadamard rotation (README item 7: natural-order
+ * Sylvester H_128, applied per 128 rows and per 128 columns; decode order
+ * H_l -> x su -> H_r -> x sv).
+ *
+ *   inverse = 0:  out = 2^-7 * H (su . W . sv) H, in the order
+ *                 x sv (columns), rows x H, x su (rows), H x columns, x 2^-7.
+ *   inverse = 1:  out = 2^-7 * su . (H W H) . sv, in the page's decode order
+ *                 H x columns, x su, rows x H, x sv, x 2^-7.
+ * H is the unnormalised Sylvester matrix, applied as radix-2 butterflies
+ * (a,b) -> (a+b, a-b) with spans 1, 2, ..., 64.  su/sv are multiplied as given;
+ * with +-1 entries the two directions are exact inverses up to rounding.
+ *
+ *   W    (device) [rows, cols], dtype `dt` (inverse = 1 requires EXL3_F32).
+ *   su   (device) fp32 [rows];  sv (device) fp32 [cols].
+ *   out  (device) fp32 [rows, cols]; must not overlap W.
+ * rows, cols: positive multiples of 128.  Pointers 16-byte aligned.
+ */
+EXL3_API exl3_status exl3_rotate(const void *W, int dt, int64_t rows, int64_t cols,
+                        const float *su, const float *sv, int inverse,
+                        float *out, void *stream);
+
+/*
+ * Workspace bytes exl3_encode_tiles needs to run n_tiles tiles at K bits with
+ * the full machine (one persistent block per SM of the current device).  A
+ * smaller workspace (at least exl3_encode_workspace_min_bytes) also works,
+ * with fewer blocks.  Returns 0 for unsupported K or n_tiles < 0.
+ */
+EXL3_API size_t exl3_encode_workspace_bytes(int64_t n_tiles, int K);
+EXL3_API size_t exl3_encode_workspace_min_bytes(int K);
+
+/*
+ * Trellis-encode every 16x16 tile of Y (README item 1: two-pass tail-biting
+ * Viterbi; item 4: 65536 >> K tracked states, candidates sigma = (k<<(16-K))|e,
+ * predecessor sigma >> K, strict-< first-branch ties; item 5: mul1 codebook,
+ * MSB-first packing with SWAP16).
+ *
+ *   Y      (device) fp32 [rows, cols], the rotated matrix; targets are
+ *          y = fl(Y * fl32(1/scale)).
+ *   rows, cols: positive multiples of 16.   K in {2, 3, 4}.   scale > 0, finite.
+ *   codes  (device, 4-byte aligned) uint16 [rows/16][cols/16][16*K].  For each
+ *          tile the codes e_i (low K bits of the chosen state at element i)
+ *          form the bitstream e_0 || e_1 || ... || e_255, each code MSB first.
+ *          Stream 16-bit word j holds bits [16j, 16j+16) (first bit = MSB) and
+ *          is stored at index j^1 (SWAP16).  Equivalently, the tile's codes
+ *          read as little-endian uint32 word m are stream bits [32m, 32m+32)
+ *          MSB first.  State i is the 16-bit window of the circular stream
+ *          ending with the last bit of e_i.
+ *   tile_cost (device) fp32 [n_tiles] or NULL: the chosen path's squared error
+ *          sum(y_i - v(s_i))^2, accumulated left to right in fp32.
+ *   ws/ws_bytes: workspace (see exl3_encode_workspace_bytes).
+ */
+EXL3_API exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K,
+                              float scale, uint16_t *codes, float *tile_cost,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Decode packed codes back to tile values (README item 5: state = circular
+ * 16-bit window, mul1 decode; item 7: values x scale before the inverse
+ * rotation).  Yhat[r, c] = fl(v(s) * scale), v the fp16 mul1 level of s.
+ *   codes (device, 4-byte aligned) as produced by exl3_encode_tiles.
+ *   Yhat  (device) fp32 [rows, cols].   rows, cols multiples of 16.
+ */
+EXL3_API exl3_status exl3_decode_tiles(const uint16_t *codes, int64_t rows, int64_t cols, int K,
+                              float scale, float *Yhat, void *stream);
+
+/*
+ * Reconstruction MSE (README item 10): sum over tiles of the fp64 squared
+ * error sum((double)W - (double)What)^2, each tile summed sequentially in
+ * row-major order and the tile sums added as a pairwise tree (neighbours
+ * (2i, 2i+1) per level, an odd last element moving up), divided by rows*cols.
+ *   W (device) dtype dt [rows, cols];  What (device) fp32 [rows, cols].
+ *   mse_out (device) one double.   rows, cols multiples of 16.
+ *   ws: at least exl3_mse_workspace_bytes(rows, cols) bytes.
+ */
+EXL3_API size_t exl3_mse_workspace_bytes(int64_t rows, int64_t cols);
+EXL3_API exl3_status exl3_mse(const void *W, int dt, const float *What, int64_t rows, int64_t cols,
+                     double *mse_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * One full quantization at relative scale g (all of the above in order):
+ * R = rotate(W); sigma = sqrt(tree(tile sums of R^2) / n) in fp64, taken as
+ * 1 when it is 0 (an all-zero matrix); s = fl32(g * sigma); codes = encode(R, s); What = inverse(decode(codes, s));
+ * mse = MSE(W, What).
+ *   W (device) bf16 or fp32 [rows, cols]; su, sv (device) fp32 sign vectors.
+ *   rows, cols multiples of 128; K in {2, 3, 4}; g > 0.
+ *   codes (device) uint16 [rows/16][cols/16][16*K].
+ *   scale_out (device) float, the absolute scale s (decode with it).
+ *   mse_out (device) double.   sigma_out (device) double or NULL.
+ *   What (device) fp32 [rows, cols] or NULL to skip writing it.
+ *   ws: exl3_quantize_workspace_bytes(rows, cols, K) for the full machine.
+ */
+EXL3_API size_t exl3_quantize_workspace_bytes(int64_t rows, int64_t cols, int K);
+EXL3_API exl3_status exl3_quantize(const void *W, int dt, int64_t rows, int64_t cols,
+                          const float *su, const float *sv, int K, double g,
+                          uint16_t *codes, float *scale_out, double *mse_out,
+                          double *sigma_out, float *What,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Golden-section search over the relative scale g in [lo, hi] (JEV-9B model
+ * card, section 2: "Golden Section Search (GSS) scale optimization"), every
+ * evaluation a full exl3_quantize.  With phi = (sqrt 5 - 1)/2 in fp64:
+ * x1 = b - phi(b-a), x2 = a + phi(b-a), both evaluated; then while fewer than
+ * n_eval evaluations: if f(x1) <= f(x2) {b = x2; x2 = x1; x1 = b - phi(b-a);
+ * evaluate x1} else {a = x1; x1 = x2; x2 = a + phi(b-a); evaluate x2}.  The
+ * result is the evaluated g with least MSE (smaller g on ties).  The search
+ * state lives on the device: the host enqueues n_eval evaluations and never
+ * waits.
+ *   lo < hi, both > 0 and finite; n_eval in [2, 64].
+ *   best_codes (device) uint16 [rows/16][cols/16][16*K]: codes at best g.
+ *   best_scale_out (device) float; best_g_out, best_mse_out (device) double.
+ *   history_out (device) double [2*n_eval] or NULL: (g, mse) per evaluation.
+ */
+EXL3_API size_t exl3_gss_workspace_bytes(int64_t rows, int64_t cols, int K);
+EXL3_API exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t cols,
+                           const float *su, const float *sv, int K,
+                           double lo, double hi, int n_eval,
+                           uint16_t *best_codes, float *best_scale_out,
+                           double *best_g_out, double *best_mse_out,
+                           double *history_out,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Profiling (no counterpart on the pages; used by the benchmark).  While
+ * enabled, each launch of the encode kernel is bracketed by two CUDA events
+ * recorded on its stream, and every kernel launch made by the library is
+ * counted.  exl3_profile_read waits for the recorded events, returns the
+ * summed encode-kernel time in milliseconds, the number of encode launches
+ * and of all kernel launches since the last read or enable, and clears them.
+ * Up to 4096 encode launches are recorded between reads.  The events belong
+ * to the device that was current at the launch.
+ */
+EXL3_API void exl3_profile_enable(int on);
+EXL3_API exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launches,
+                              int64_t *kernel_launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_H */

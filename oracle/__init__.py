@@ -308,7 +308,10 @@ def mse(W, What) -> float:
 
 
 def scale_for(g: float, sigma: float) -> tuple[float, float]:
-    """(s, inv_s): s = fl32(g * sigma) (product in fp64), inv_s = fl32(1 / s)."""
+    """(s, inv_s): s = fl32(g * sigma) (product in fp64), inv_s = fl32(1 / s).
+    An all-zero matrix (sigma == 0) is coded at sigma = 1."""
+    if sigma == 0.0:
+        sigma = 1.0
     s = np.float32(float(g) * float(sigma))
     inv = np.float32(1.0) / s
     return float(s), float(inv)

@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI (not gpu): the library loads, exports every
+symbol include/exl3.h declares, and rejects bad arguments before touching the
+GPU.  Only invalid-argument paths are exercised, with fake pointers that the
+library never dereferences."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ex():
+    import __graft_entry__
+    from exl3_trellis_weight_gb300 import build
+    build.build()
+    import exl3_trellis_weight_gb300 as ex
+    ex.lib()
+    return ex
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "exl3.h")).read()
+    return sorted(set(re.findall(r"EXL3_API[^;(]*?\b(exl3_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_path(ex):
+    names = _declared()
+    for n in ["exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_gss_scale",
+              "exl3_quantize", "exl3_mse"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(ex):
+    L = ex.lib()
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(ex):
+    L = ex.lib()
+    assert L.exl3_status_str(0) == b"EXL3_OK"
+    assert L.exl3_status_str(3) == b"EXL3_ERR_WORKSPACE"
+    assert L.exl3_status_str(99) == b"EXL3_ERR_UNKNOWN"
+    assert L.exl3_version() >= 100
+
+
+def test_supported_k(ex):
+    assert [ex.supports_k(k) for k in range(0, 6)] == [False, False, True, True, True, False]
+
+
+FAKE = ctypes.c_void_p(0x10000000)      # 256-byte aligned, never dereferenced
+
+
+def test_encode_rejects_bad_arguments(ex):
+    L = ex.lib()
+    ws_min = ex.encode_workspace_min_bytes(2)
+    assert ws_min > 0
+    args = dict(Y=FAKE, rows=64, cols=64, K=2, scale=ctypes.c_float(1.0), codes=FAKE,
+                cost=None, ws=FAKE, ws_bytes=ws_min, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.exl3_encode_tiles(a["Y"], a["rows"], a["cols"], a["K"], a["scale"], a["codes"],
+                                   a["cost"], a["ws"], a["ws_bytes"], a["stream"])
+
+    assert call(K=1) == 2 and call(K=5) == 2               # unsupported K
+    assert call(rows=40) == 2 and call(cols=24) == 2       # not multiples of 16
+    assert call(rows=0) == 1 and call(cols=-16) == 1
+    assert call(Y=None) == 1 and call(codes=None) == 1
+    assert call(codes=ctypes.c_void_p(0x10000002)) == 1    # misaligned
+    assert call(scale=ctypes.c_float(0.0)) == 1
+    assert call(scale=ctypes.c_float(float("inf"))) == 1
+    assert call(scale=ctypes.c_float(float("nan"))) == 1
+    assert call(ws_bytes=ws_min - 1) == 3                   # workspace too small
+    assert call(ws=None) == 1
+    assert call(ws=ctypes.c_void_p(0x10000010)) == 1        # workspace not 256-aligned
+    assert b"workspace" in L.exl3_last_error()
+
+
+def test_rotate_and_quantize_reject_bad_arguments(ex):
+    L = ex.lib()
+    # rows/cols must be multiples of 128 for the rotation
+    assert L.exl3_rotate(FAKE, 1, 64, 128, FAKE, FAKE, 0, ctypes.c_void_p(0x20000000), None) == 2
+    assert L.exl3_rotate(FAKE, 7, 128, 128, FAKE, FAKE, 0, ctypes.c_void_p(0x20000000), None) == 1
+    assert L.exl3_rotate(FAKE, 1, 128, 128, FAKE, FAKE, 1, ctypes.c_void_p(0x20000000), None) == 1
+    assert L.exl3_rotate(FAKE, 0, 128, 128, None, FAKE, 0, ctypes.c_void_p(0x20000000), None) == 1
+    # overlapping output
+    assert L.exl3_rotate(FAKE, 1, 128, 128, FAKE, FAKE, 0, ctypes.c_void_p(0x10000100), None) == 1
+    ws = ex.quantize_workspace_bytes(256, 256, 2)
+    assert ws > 0
+    q = lambda **kw: L.exl3_quantize(FAKE, 1, kw.get("rows", 256), 256, FAKE, FAKE, kw.get("K", 2),
+                                     ctypes.c_double(kw.get("g", 1.0)), FAKE, FAKE, FAKE, None, None,
+                                     FAKE, kw.get("ws", ws), None)
+    assert q(K=3, g=-1.0) == 1
+    assert q(g=float("nan")) == 1
+    assert q(rows=200) == 2
+    assert q(K=7) == 2
+    assert q(ws=1000) == 3
+    gws = ex.gss_workspace_bytes(256, 256, 2)
+    gs = lambda lo, hi, n, w=gws: L.exl3_gss_scale(FAKE, 1, 256, 256, FAKE, FAKE, 2,
+                                                   ctypes.c_double(lo), ctypes.c_double(hi), n,
+                                                   FAKE, FAKE, FAKE, FAKE, None, FAKE, w, None)
+    assert gs(0.5, 2.0, 1) == 1
+    assert gs(0.5, 2.0, 65) == 1
+    assert gs(2.0, 0.5, 12) == 1
+    assert gs(0.0, 2.0, 12) == 1
+    assert gs(0.5, 2.0, 12, w=100) == 3
+
+
+def test_workspace_queries_scale_with_work(ex):
+    a = ex.encode_workspace_bytes(10, 2)
+    b = ex.encode_workspace_bytes(100000, 2)
+    assert 0 < a <= b
+    assert a == 10 * ex.encode_workspace_min_bytes(2)
+    assert ex.encode_workspace_bytes(100, 1) == 0
+    assert ex.quantize_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
+    assert ex.gss_workspace_bytes(4096, 4096, 2) > ex.quantize_workspace_bytes(4096, 4096, 2)

@@ -1,0 +1,334 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Codes, decoded values, rotations and tile costs must be bit-exact; the scale
+and the MSE are compared within 1e-6 relative (the fixed reduction order makes
+them exact in practice, and the tests also record that).  Inputs come from the
+seeded generators in exl3_trellis_weight_gb300.inputs and reach both sides as
+the same bytes.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from exl3_trellis_weight_gb300 import inputs  # noqa: E402
+
+REL_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def ex():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is required for -m gpu tests")
+    import __graft_entry__
+    __graft_entry__.build()
+    import exl3_trellis_weight_gb300 as ex
+    return ex
+
+
+DEV = "cuda:0"
+
+
+def _np_codes(codes_t, K):
+    return codes_t.detach().cpu().numpy().view(np.uint16).reshape(-1, 16 * K)
+
+
+def _oracle_codes(Y, K, inv_scale, tiles=None):
+    st, costs = oracle.encode_matrix(Y, K, inv_scale, tiles=tiles)
+    return np.stack([oracle.pack(s, K) for s in st]), costs
+
+
+def _tiles_of(rows, cols):
+    return (rows // 16) * (cols // 16)
+
+
+# ---------------------------------------------------------------------------
+# encode: small cases, all tiles
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def rot128():
+    (_, W, _, _, _), = inputs.workload("rot128_iid_k2")
+    return W.numpy()
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_encode_rot128_bit_exact(ex, rot128, K):
+    Y = rot128
+    codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=1.0, want_cost=True)
+    torch.cuda.synchronize()
+    want, wcost = _oracle_codes(Y, K, 1.0)
+    got = _np_codes(codes, K)
+    assert np.array_equal(got, want)
+    assert np.array_equal(cost.cpu().numpy().view(np.uint32), wcost.view(np.uint32))
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("blocks", [None, 1, 4])
+def test_encode_ragged_tiles_and_small_grids(ex, K, blocks):
+    """15 tiles (3x5, not a multiple of the pair pipeline); 1 block walks all
+    15 (odd count, drain phase), 4 blocks take 4/4/4/3."""
+    rng = np.random.default_rng(10 + K)
+    Y = rng.standard_normal((48, 80)).astype(np.float32) * 0.7
+    ws = None
+    if blocks is not None:
+        ws = torch.empty(blocks * ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
+    codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=0.7, want_cost=True, ws=ws)
+    torch.cuda.synchronize()
+    inv = float(np.float32(1.0) / np.float32(0.7))
+    want, wcost = _oracle_codes(Y, K, inv)
+    assert np.array_equal(_np_codes(codes, K), want)
+    assert np.array_equal(cost.cpu().numpy().view(np.uint32), wcost.view(np.uint32))
+
+
+def _edge_inputs():
+    rng = np.random.default_rng(5)
+    cb = oracle.mul1_table()
+    yield "zeros", np.zeros((16, 64), np.float32)
+    yield "constant", np.full((16, 64), 0.37, np.float32)
+    yield "tiny", (rng.standard_normal((16, 64)) * 1e-30).astype(np.float32)
+    yield "outliers", np.where(rng.random((16, 64)) < 0.05, 1e4, rng.standard_normal((16, 64))).astype(np.float32)
+    # targets exactly on codebook levels: many exact ties between paths
+    yield "levels", cb[rng.integers(0, 65536, (16, 64))].astype(np.float32)
+    yield "two_levels", np.where(rng.random((16, 64)) < 0.5, cb[1], cb[2]).astype(np.float32)
+
+
+@pytest.mark.parametrize("name,Y", list(_edge_inputs()), ids=[n for n, _ in _edge_inputs()])
+@pytest.mark.parametrize("K", [2, 4])
+def test_encode_edge_inputs_bit_exact(ex, name, Y, K):
+    codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=1.0, want_cost=True)
+    torch.cuda.synchronize()
+    want, wcost = _oracle_codes(Y, K, 1.0)
+    assert np.array_equal(_np_codes(codes, K), want), name
+    assert np.array_equal(cost.cpu().numpy().view(np.uint32), wcost.view(np.uint32)), name
+
+
+def test_encode_single_tile_and_repeatability(ex):
+    rng = np.random.default_rng(99)
+    Y = rng.standard_normal((16, 16)).astype(np.float32)
+    a = ex.encode_tiles(torch.from_numpy(Y).to(DEV), 3)
+    b = ex.encode_tiles(torch.from_numpy(Y).to(DEV), 3)
+    torch.cuda.synchronize()
+    want, _ = _oracle_codes(Y, 3, 1.0)
+    assert np.array_equal(_np_codes(a, 3), want)
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# decode, rotation, MSE
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_decode_random_codes_bit_exact(ex, K):
+    rows, cols = 512, 1024 if K == 4 else 256
+    rng = np.random.default_rng(K)
+    n = _tiles_of(rows, cols)
+    codes = rng.integers(0, 1 << 16, (n, 16 * K), dtype=np.uint64).astype(np.uint16)
+    scale = 0.0123
+    got = ex.decode_tiles(torch.from_numpy(codes.view(np.int16)).to(DEV).reshape(rows // 16, cols // 16, 16 * K),
+                          rows, cols, K, scale)
+    torch.cuda.synchronize()
+    want = oracle.decode_matrix(codes, rows, cols, K, scale)
+    assert np.array_equal(got.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    if K == 4:
+        # 2^20 windows: (nearly) every state's level went through the comparison
+        states = np.concatenate([oracle.unpack_states(codes[t], K) for t in range(0, n, 1)])
+        assert np.unique(states).size > 65000
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_rotate_forward_and_inverse_bit_exact(ex, dt):
+    rows, cols = 256, 384
+    W = inputs.linear_bf16(rows, cols, seed=3, std=0.02)
+    if dt == "f32":
+        W = (W.float() + torch.randn(rows, cols, generator=torch.Generator().manual_seed(4)) * 1e-3)
+    su, sv = inputs.sign_pair(rows, cols, 3)
+    R = ex.rotate(W.to(DEV), su.to(DEV), sv.to(DEV))
+    torch.cuda.synchronize()
+    Wf = W.float().numpy()
+    want = oracle.rotate_forward(Wf, su.numpy(), sv.numpy())
+    assert np.array_equal(R.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    back = ex.rotate(R, su.to(DEV), sv.to(DEV), inverse=True)
+    torch.cuda.synchronize()
+    want_b = oracle.rotate_inverse(want, su.numpy(), sv.numpy())
+    assert np.array_equal(back.cpu().numpy().view(np.uint32), want_b.view(np.uint32))
+
+
+def test_rotate_in_place_fp32(ex):
+    rows, cols = 128, 256
+    W = torch.randn(rows, cols, generator=torch.Generator().manual_seed(8))
+    su, sv = inputs.sign_pair(rows, cols, 8)
+    want = oracle.rotate_forward(W.numpy(), su.numpy(), sv.numpy())
+    Wd = W.to(DEV)
+    ex.rotate(Wd, su.to(DEV), sv.to(DEV), out=Wd)
+    torch.cuda.synchronize()
+    assert np.array_equal(Wd.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_mse_fixed_order(ex, dt):
+    rows, cols = 256, 512
+    W = inputs.linear_bf16(rows, cols, seed=11)
+    if dt == "f32":
+        W = W.float()
+    What = (W.float() + torch.randn(rows, cols, generator=torch.Generator().manual_seed(12)) * 1e-3)
+    m = ex.mse(W.to(DEV), What.to(DEV))
+    torch.cuda.synchronize()
+    want = oracle.mse(W.float().numpy(), What.numpy())
+    got = float(m.item())
+    assert abs(got - want) <= REL_TOL * want
+    assert got == want   # same per-tile order and tree
+
+
+# ---------------------------------------------------------------------------
+# full chain and golden-section search
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols,K,seed", [(256, 256, 2, 21), (128, 256, 3, 22), (256, 128, 4, 23)])
+def test_quantize_chain_matches_oracle(ex, rows, cols, K, seed):
+    W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02, outlier_frac=0.001)
+    su, sv = inputs.sign_pair(rows, cols, seed)
+    res = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K, g=1.1, want_What=True)
+    torch.cuda.synchronize()
+    ref = oracle.evaluate_matrix(W.float().numpy(), su.numpy(), sv.numpy(), K, 1.1)
+    assert np.array_equal(_np_codes(res["codes"], K), ref["codes"].reshape(-1, 16 * K))
+    assert float(res["scale"].item()) == ref["scale"]
+    assert float(res["sigma"].item()) == ref["sigma"]
+    assert np.array_equal(res["What"].cpu().numpy().view(np.uint32), ref["What"].view(np.uint32))
+    got = float(res["mse"].item())
+    assert abs(got - ref["mse"]) <= REL_TOL * ref["mse"]
+
+
+def test_quantize_zero_matrix(ex):
+    W = torch.zeros(128, 128, dtype=torch.bfloat16)
+    su, sv = inputs.sign_pair(128, 128, 1)
+    res = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), 2, g=1.0)
+    torch.cuda.synchronize()
+    ref = oracle.evaluate_matrix(W.float().numpy(), su.numpy(), sv.numpy(), 2, 1.0)
+    assert np.array_equal(_np_codes(res["codes"], 2), ref["codes"].reshape(-1, 32))
+    assert float(res["scale"].item()) == ref["scale"] == 1.0
+    assert float(res["mse"].item()) == ref["mse"]
+
+
+def test_quantize_small_workspace_same_result(ex):
+    rows, cols, K = 256, 256, 2
+    W = inputs.linear_bf16(rows, cols, seed=31)
+    su, sv = inputs.sign_pair(rows, cols, 31)
+    full = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = min(_tiles_of(rows, cols), sms)
+    fixed = ex.quantize_workspace_bytes(rows, cols, K) - grid * ex.encode_workspace_min_bytes(K)
+    ws = torch.empty(fixed + 3 * ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
+    small = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(full["codes"], small["codes"])
+    assert float(full["mse"].item()) == float(small["mse"].item())
+
+
+def test_gss_matches_oracle_search(ex):
+    rows, cols, K = 128, 128, 2
+    W = inputs.linear_bf16(rows, cols, seed=41, std=0.02)
+    su, sv = inputs.sign_pair(rows, cols, 41)
+    res = ex.gss_scale(W.to(DEV), su.to(DEV), sv.to(DEV), K, 0.5, 2.0, 12, want_history=True)
+    torch.cuda.synchronize()
+    Wf, sun, svn = W.float().numpy(), su.numpy(), sv.numpy()
+    cache = {}
+
+    def f(g):
+        cache[g] = oracle.evaluate_matrix(Wf, sun, svn, K, g)
+        return cache[g]["mse"]
+
+    best_g, best_f, hist = oracle.golden_section_search(f, 0.5, 2.0, 12)
+    h = res["history"].cpu().numpy().reshape(-1, 2)
+    assert np.array_equal(h[:, 0], np.array([x for x, _ in hist]))
+    assert np.allclose(h[:, 1], np.array([y for _, y in hist]), rtol=REL_TOL, atol=0)
+    assert float(res["g"].item()) == best_g
+    assert abs(float(res["mse"].item()) - best_f) <= REL_TOL * best_f
+    assert float(res["scale"].item()) == cache[best_g]["scale"]
+    assert np.array_equal(_np_codes(res["codes"], K), cache[best_g]["codes"].reshape(-1, 16 * K))
+
+
+# ---------------------------------------------------------------------------
+# full workload sizes, launch configuration of the benchmark, sampled tiles
+# ---------------------------------------------------------------------------
+
+def _sample_tiles(n, k, seed):
+    rng = np.random.default_rng(seed)
+    fixed = np.array([0, 1, n - 1, n // 2, n - 2], dtype=np.int64)
+    return np.unique(np.concatenate([fixed, rng.choice(n, k, replace=False)]))
+
+
+def _check_full(ex, W, su, sv, K, n_sample, seed):
+    rows, cols = W.shape
+    res = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K, g=1.0)
+    torch.cuda.synchronize()
+    Wf = W.float().numpy()
+    R = oracle.rotate_forward(Wf, su.numpy(), sv.numpy())
+    sigma = oracle.rms(R)
+    s, inv = oracle.scale_for(1.0, sigma)
+    assert float(res["sigma"].item()) == sigma
+    assert float(res["scale"].item()) == s
+    idx = _sample_tiles(_tiles_of(rows, cols), n_sample, seed)
+    want, _ = _oracle_codes(R, K, inv, tiles=idx)
+    got = _np_codes(res["codes"], K)[idx]
+    assert np.array_equal(got, want)
+    return res
+
+
+def test_full_linear4096_k2_sampled(ex):
+    (_, W, su, sv, K), = inputs.workload("linear4096_k2")
+    res = _check_full(ex, W, su, sv, K, 48, 1)
+    m = float(res["mse"].item())
+    assert 0 < m < float(W.float().var())
+
+
+def test_full_mlp12288_k4_sampled(ex):
+    (_, W, su, sv, K), = inputs.workload("mlp12288_t5_k4")
+    _check_full(ex, W, su, sv, K, 24, 2)
+
+
+@pytest.mark.parametrize("proj", ["k", "down"])
+def test_full_layer_k3_sampled(ex, proj):
+    for lab, W, su, sv, K in inputs.workload("layer4096_k3"):
+        if lab == proj:
+            _check_full(ex, W, su, sv, K, 16, 3)
+
+
+def test_full_gss4096_k2(ex):
+    """12-evaluation search on 4096x4096: the state machine reproduces the
+    oracle's points given the measured MSEs; the best codes equal a fresh
+    quantize at the best g; sampled tiles match the oracle at that scale."""
+    (_, W, su, sv, K), = inputs.workload("gss4096_k2")
+    Wd, sud, svd = W.to(DEV), su.to(DEV), sv.to(DEV)
+    res = ex.gss_scale(Wd, sud, svd, K, 0.5, 2.0, 12, want_history=True)
+    torch.cuda.synchronize()
+    h = res["history"].cpu().numpy().reshape(-1, 2)
+    lookup = {float(x): float(y) for x, y in h}
+    best_g, best_f, hist = oracle.golden_section_search(lambda g: lookup[g], 0.5, 2.0, 12)
+    assert [x for x, _ in hist] == [float(x) for x in h[:, 0]]
+    assert float(res["g"].item()) == best_g and float(res["mse"].item()) == best_f
+    again = ex.quantize(Wd, sud, svd, K, g=best_g)
+    torch.cuda.synchronize()
+    assert torch.equal(again["codes"], res["codes"])
+    assert float(again["mse"].item()) == best_f
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    s, inv = oracle.scale_for(best_g, oracle.rms(R))
+    assert float(res["scale"].item()) == s
+    idx = _sample_tiles(_tiles_of(*W.shape), 16, 4)
+    want, _ = _oracle_codes(R, K, inv, tiles=idx)
+    assert np.array_equal(_np_codes(res["codes"], K)[idx], want)
+
+
+def test_profile_counts_launches(ex):
+    rows, cols, K = 256, 256, 2
+    W = inputs.linear_bf16(rows, cols, seed=51)
+    su, sv = inputs.sign_pair(rows, cols, 51)
+    ex.profile_enable(True)
+    ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K)
+    ms, n_enc, n_all = ex.profile_read()
+    ex.profile_enable(False)
+    assert n_enc == 1 and ms > 0
+    assert n_all >= 7
