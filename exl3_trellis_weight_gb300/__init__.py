@@ -126,10 +126,12 @@ def _dt(t) -> int:
 
 
 def _workspace(nbytes: int, device, ws=None):
+    """A caller-supplied workspace is passed through as is: the library accepts
+    anything from its per-call minimum up (fewer encode blocks when smaller)
+    and returns EXL3_ERR_WORKSPACE below that."""
     torch = _torch()
     if ws is not None:
-        if ws.numel() * ws.element_size() < nbytes:
-            raise ValueError(f"workspace too small: need {nbytes} bytes")
+        _need_cuda(ws)
         return ws
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
