@@ -1,0 +1,57 @@
+"""Small, named launches of one kernel family each, for profiler captures.
+
+    python -m exl3_trellis_weight_gb300.profile_cases encode --K 2 --rows 1216 --cols 256
+    python -m exl3_trellis_weight_gb300.profile_cases rotate --rows 4096 --cols 4096
+
+encode : exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1.
+rotate : exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix.
+Each case runs --reps launches and synchronises; it prints the wall time.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None) -> int:
+    import torch
+    import exl3_trellis_weight_gb300 as ex
+    from exl3_trellis_weight_gb300 import build, inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["encode", "rotate"])
+    ap.add_argument("--K", type=int, default=2)
+    ap.add_argument("--rows", type=int, default=1216)
+    ap.add_argument("--cols", type=int, default=256)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    build.build()
+    dev = torch.device("cuda:0")
+    if a.case == "encode":
+        Y = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+        n = (a.rows // 16) * (a.cols // 16)
+        ws = torch.empty(ex.encode_workspace_bytes(n, a.K), dtype=torch.uint8, device=dev)
+        codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
+        fn = lambda: ex.encode_tiles(Y, a.K, 1.0, codes=codes, ws=ws)
+    else:
+        W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
+        su, sv = (t.to(dev) for t in inputs.sign_pair(a.rows, a.cols, 0))
+        out = torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev)
+        fn = lambda: ex.rotate(W, su, sv, out=out)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(a.reps):
+        fn()
+    torch.cuda.synchronize()
+    print(f"{a.case}: {a.reps} launches, {1e3 * (time.perf_counter() - t0) / a.reps:.3f} ms each")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
