@@ -337,7 +337,28 @@ exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s) {
     return cuda_check(cudaGetLastError(), "encode launch");
 }
 
+template <int K>
+exl3_status launch_k_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
+    using Gm = Geo<K>;
+    const size_t smem = (size_t)(2 * Gm::G + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(encode_kernel<K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaFuncSetAttribute(encode)");
+    encode_kernel<K><<<p.grid, kThreads, smem, s>>>(p);
+    return cuda_check(cudaGetLastError(), "encode launch");
+}
+
 }  // namespace
+
+exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
+    switch (p.K) {
+    case 2: return launch_k_unprofiled<2>(p, s);
+    case 3: return launch_k_unprofiled<3>(p, s);
+    case 4: return launch_k_unprofiled<4>(p, s);
+    default: return set_error(EXL3_ERR_UNSUPPORTED, "K=%d is not built", p.K);
+    }
+}
 
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s) {
     switch (p.K) {

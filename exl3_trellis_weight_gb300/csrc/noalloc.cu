@@ -1,0 +1,104 @@
+// noalloc.cu -- exl3_encode_tiles_noalloc: the trellis encode for callers that
+// cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: plug-ins that run inside a host
+// application which owns every byte of device memory through its own pool, and
+// latency-critical loops where an allocation (which can synchronise the whole
+// device) is not acceptable.  They cannot provide the encoder's workspace either
+// if they have no pool of their own to carve it from.  For them the decision
+// rows of the encoder live in one file-scope device array instead.
+//
+// The array holds the decision rows of up to kNoAllocMaxBlocks persistent encode
+// blocks (3 MiB each, 24 MiB in total).  It is created when the library's code
+// is loaded on a device and stays allocated on every device that loads the
+// library until the process exits.  Its host-side name is only a stand-in: the
+// device address is looked up once per device with cudaGetSymbolAddress.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kNoAllocMaxBlocks = EXL3_NOALLOC_MAX_BLOCKS;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[(size_t)kNoAllocMaxBlocks *
+                                                            kEncodeBlockScratchBytes /
+                                                            sizeof(uint32_t)];
+
+std::mutex g_mu;
+uint32_t *g_addr[kMaxDevices] = {};
+
+// Device address of the scratch array for the current device (set-up on the
+// first call per device).
+exl3_status scratch_address(uint32_t **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(EXL3_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_check(e, "cudaGetSymbolAddress(noalloc scratch)");
+        g_addr[dev] = static_cast<uint32_t *>(p);
+    }
+    *out = g_addr[dev];
+    return EXL3_OK;
+}
+
+}  // namespace
+}  // namespace exl3
+
+using namespace exl3;
+
+extern "C" EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_t rows,
+                                                          int64_t cols, int K, float scale,
+                                                          uint16_t *codes, float *tile_cost,
+                                                          int blocks, void *stream) {
+    if (!Y || !codes)
+        return set_error(EXL3_ERR_INVALID_ARG, "Y and codes must not be NULL");
+    if (((uintptr_t)Y % 4) || ((uintptr_t)codes % 4) || ((uintptr_t)tile_cost % 4))
+        return set_error(EXL3_ERR_INVALID_ARG, "Y, codes and tile_cost must be 4-byte aligned");
+    if (rows <= 0 || cols <= 0)
+        return set_error(EXL3_ERR_INVALID_ARG, "rows and cols must be positive");
+    if (rows % 16 || cols % 16)
+        return set_error(EXL3_ERR_UNSUPPORTED, "rows=%lld cols=%lld must be multiples of 16",
+                         (long long)rows, (long long)cols);
+    if (rows > (1ll << 24) || cols > (1ll << 24) || rows * cols > (1ll << 34))
+        return set_error(EXL3_ERR_INVALID_ARG, "matrix %lldx%lld is too large", (long long)rows,
+                         (long long)cols);
+    if (K < 2 || K > 4)
+        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: this build encodes K in {2,3,4}", K);
+    if (!(scale > 0.0f) || !(scale < __builtin_inff()))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (blocks < 0 || blocks > kNoAllocMaxBlocks)
+        return set_error(EXL3_ERR_WORKSPACE,
+                         "blocks=%d exceeds the static scratch: at most %d blocks (%zu bytes each)",
+                         blocks, kNoAllocMaxBlocks, kEncodeBlockScratchBytes);
+    uint32_t *scratch = nullptr;
+    exl3_status st = scratch_address(&scratch);
+    if (st != EXL3_OK)
+        return st;
+    const int64_t n_tiles = (rows / 16) * (cols / 16);
+    int64_t grid = blocks == 0 ? kNoAllocMaxBlocks : blocks;
+    if (grid > n_tiles)
+        grid = n_tiles;
+    EncodeLaunch el{};
+    el.Y = Y;
+    el.rows = rows;
+    el.cols = cols;
+    el.K = K;
+    el.inv_scale = 1.0f / scale;
+    el.inv_scale_dev = nullptr;
+    el.codes = reinterpret_cast<uint32_t *>(codes);
+    el.tile_cost = tile_cost;
+    el.scratch = scratch;   // every decision row is written before it is read
+    el.grid = (int)grid;
+    return launch_encode_unprofiled(el, (cudaStream_t)stream);
+}

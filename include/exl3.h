@@ -197,6 +197,35 @@ EXL3_API exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t
                            void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * exl3_encode_tiles without a workspace, for callers that cannot allocate
+ * device memory (no counterpart on the pages: an interface addition of this
+ * library).  Such callers include plug-ins running inside an application that
+ * owns all device memory through its own pool, and latency-critical loops that
+ * cannot afford an allocation (cudaMalloc may synchronise the whole device).
+ *
+ * Same inputs, outputs, layout and results as exl3_encode_tiles; the decision
+ * rows live in a static device array inside the library instead of a caller
+ * workspace.  That array holds at most EXL3_NOALLOC_MAX_BLOCKS persistent
+ * blocks (8 blocks x 3,137,536 bytes, about 24 MiB) and stays allocated on every
+ * device that loads the library until the process exits.
+ *   blocks: number of persistent blocks to run, 1..EXL3_NOALLOC_MAX_BLOCKS, or
+ *           0 for the maximum.  More is rejected with EXL3_ERR_WORKSPACE.
+ *           With at most 8 of the GPU's SMs busy this is slower than
+ *           exl3_encode_tiles with a full-machine workspace.
+ * The first call on each device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The function allocates nothing and creates no CUDA events.  All
+ * calls share the one array: calls whose work overlaps on the GPU (for example
+ * on two streams without ordering) race and produce wrong codes.  Nothing in
+ * the array needs clearing between calls: each call writes every decision row
+ * before reading it.
+ */
+#define EXL3_NOALLOC_MAX_BLOCKS 8
+EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_t rows, int64_t cols, int K,
+                                               float scale, uint16_t *codes, float *tile_cost,
+                                               int blocks, void *stream);
+
+/*
  * Profiling (no counterpart on the pages; used by the benchmark).  While
  * enabled, each launch of the encode kernel is bracketed by two CUDA events
  * recorded on its stream, and every kernel launch made by the library is
