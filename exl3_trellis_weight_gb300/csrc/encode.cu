@@ -28,12 +28,6 @@ namespace exl3 {
 
 namespace {
 
-__device__ __forceinline__ float half_at(const uint32_t (&vpk)[32], int idx) {
-    const uint32_t w = vpk[idx >> 1];
-    const unsigned short h = (idx & 1) ? (unsigned short)(w >> 16) : (unsigned short)(w & 0xFFFFu);
-    return __half2float(__ushort_as_half(h));
-}
-
 template <int K>
 __device__ __forceinline__ void put_code(uint32_t *bs, int t, uint32_t e) {
     const int p = t * K;
@@ -56,10 +50,86 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
     return v;
 }
 
+// fl(v - y) with v an fp16 value held in 16 bits (one mixed-precision subtract;
+// exact widening of v, one binary32 rounding).  (v - y)^2 == (y - v)^2 bitwise.
+__device__ __forceinline__ float sub_h_f(unsigned short v, float y) {
+    float r;
+    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(v), "f"(y));
+    return r;
+}
+
+// Two independent binary32 multiplies in one instruction.
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+
+// Candidate k of a pair of tracked entries (jj, jj+1) sharing predecessor cost
+// mk: c = fl(mk + fl(fl(v - y)^2)) for both.  The square of the pair runs as one
+// f32x2 multiply; the add stays scalar, because the compiler contracts a packed
+// multiply feeding a packed add into a fused multiply-add whatever the rounding
+// qualifiers, and a fused result differs from the two-rounding definition.
+__device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, const float y,
+                                          int &c0, int &c1) {
+    const float d0 = sub_h_f((unsigned short)(vw & 0xFFFFu), y);
+    const float d1 = sub_h_f((unsigned short)(vw >> 16), y);
+    const unsigned long long dd = pack2(d0, d1);
+    const unsigned long long q = mul2(dd, dd);
+    c0 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q & 0xffffffffull))));
+    c1 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q >> 32))));
+}
+
+// Candidate k of the pair, then the running minimum (ties keep the lower k).
+__device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
+                                         int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
+    int c0, c1;
+    cand_pair(mk, vw, y, c0, c1);
+    if (k == 0) {
+        best0 = c0;
+        best1 = c1;
+        bk0 = 0u;
+        bk1 = 0u;
+    } else {
+        bool keep0, keep1;
+        best0 = __vibmin_s32(best0, c0, &keep0);   // keep0: best0 <= c0
+        best1 = __vibmin_s32(best1, c1, &keep1);
+        bk0 = keep0 ? bk0 : (uint32_t)k;
+        bk1 = keep1 ? bk1 : (uint32_t)k;
+    }
+}
+
+template <int K, bool ARGMIN>
+__device__ __forceinline__ void finish_pair(const int u, const int jp, const int hp, const int j0,
+                                            const int best0, const int best1, const uint32_t bk0,
+                                            const uint32_t bk1, float *outv, uint32_t &word,
+                                            unsigned long long &key) {
+    using Gm = Geo<K>;
+    outv[jp] = __int_as_float(best0);
+    outv[jp + 1] = __int_as_float(best1);
+    word |= (bk0 << ((u * Gm::NJ + jp) * K)) | (bk1 << ((u * Gm::NJ + jp + 1) * K));
+    if (ARGMIN) {
+        const uint32_t g0 = ((uint32_t)hp << K) | (uint32_t)(j0 + jp);
+        const unsigned long long k0 =
+            ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << Gm::KR) | g0);
+        const unsigned long long k1 =
+            ((unsigned long long)(uint32_t)best1 << 32) | ((bk1 << Gm::KR) | (g0 + 1u));
+        key = k0 < key ? k0 : key;
+        key = k1 < key ? k1 : key;
+    }
+}
+
 // One add-compare-select step over the thread's 64 candidate states.
 //   M_t(g) = min_k fl(M_{t-1}((k << (16-2K)) | (g >> K)) + fl(fl(y - v)^2)),
-// lowest k on ties.  Writes the thread's decision word; with ARGMIN, instead
-// of storing M_t it folds (cost, full state index) of each tracked entry into
+// lowest k on ties.  Tracked entries are handled in pairs (jj, jj+1), which
+// share their predecessor costs.  Costs are non-negative binary32 values (or
+// +inf), whose bit patterns order like signed integers: the running minimum is
+// the DPX min-with-predicate, keeping the earlier (lower k) candidate on ties.
+// Writes the thread's decision word (K bits per entry); with ARGMIN, instead of
+// storing M_t it folds (cost, full state index) of each tracked entry into
 // `key` (lexicographic minimum).
 template <int K, bool ARGMIN>
 __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__restrict__ Mn,
@@ -71,48 +141,46 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
     for (int u = 0; u < Gm::NU; u++) {
         const int hp = Gm::unit(u, tid);
         const int j0 = Gm::j0(tid);
-        float m[Gm::NK];
-#pragma unroll
-        for (int k = 0; k < Gm::NK; k++)
-            m[k] = Mp[(k << (16 - 2 * K)) | hp];
         float outv[Gm::NJ];
+        if (Gm::NK <= 2 * Gm::NJ) {
+            // predecessor costs live (NK registers), one pair of entries at a time
+            float m[Gm::NK];
 #pragma unroll
-        for (int jj = 0; jj < Gm::NJ; jj++) {
-            float best = 0.0f;
-            uint32_t bk = 0u;
+            for (int k = 0; k < Gm::NK; k++)
+                m[k] = Mp[(k << (16 - 2 * K)) | hp];
+#pragma unroll
+            for (int jp = 0; jp < Gm::NJ; jp += 2) {
+                int best0 = 0, best1 = 0;
+                uint32_t bk0 = 0u, bk1 = 0u;
+#pragma unroll
+                for (int k = 0; k < Gm::NK; k++)
+                    acs_pair(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1,
+                             bk0, bk1);
+                finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
+            }
+        } else {
+            // running minima of all entries live (2*NJ registers), one cost at a time
+            int best[Gm::NJ];
+            uint32_t bk[Gm::NJ];
 #pragma unroll
             for (int k = 0; k < Gm::NK; k++) {
-                const float v = half_at(vpk, (u * Gm::NK + k) * Gm::NJ + jj);
-                const float d = __fsub_rn(y, v);
-                const float c = __fadd_rn(m[k], __fmul_rn(d, d));
-                if (k == 0) {
-                    best = c;
-                } else if (c < best) {
-                    best = c;
-                    bk = (uint32_t)k;
-                }
+                const float mk = Mp[(k << (16 - 2 * K)) | hp];
+#pragma unroll
+                for (int jp = 0; jp < Gm::NJ; jp += 2)
+                    acs_pair(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best[jp],
+                             best[jp + 1], bk[jp], bk[jp + 1]);
             }
-            outv[jj] = best;
-            word |= bk << ((u * Gm::NJ + jj) * K);
-            if (ARGMIN) {
-                const uint32_t g = ((uint32_t)hp << K) | (uint32_t)(j0 + jj);
-                const uint32_t full = (bk << Gm::KR) | g;
-                const unsigned long long kk =
-                    ((unsigned long long)__float_as_uint(best) << 32) | full;
-                key = kk < key ? kk : key;
-            }
+#pragma unroll
+            for (int jp = 0; jp < Gm::NJ; jp += 2)
+                finish_pair<K, ARGMIN>(u, jp, hp, j0, best[jp], best[jp + 1], bk[jp], bk[jp + 1],
+                                       outv, word, key);
         }
         if (!ARGMIN) {
             float *dst = Mn + (((uint32_t)hp << K) | (uint32_t)j0);
-            if (Gm::NJ == 2) {
-                *reinterpret_cast<float2 *>(dst) = make_float2(outv[0], outv[1 % Gm::NJ]);
-            } else {
 #pragma unroll
-                for (int q = 0; q < Gm::NJ; q += 4)
-                    *reinterpret_cast<float4 *>(dst + q) =
-                        make_float4(outv[q], outv[(q + 1) % Gm::NJ], outv[(q + 2) % Gm::NJ],
-                                    outv[(q + 3) % Gm::NJ]);
-            }
+            for (int q = 0; q < Gm::NJ; q += 4)
+                *reinterpret_cast<float4 *>(dst + q) =
+                    make_float4(outv[q], outv[q + 1], outv[q + 2], outv[q + 3]);
         }
     }
 }
