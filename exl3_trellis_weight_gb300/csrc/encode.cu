@@ -73,21 +73,37 @@ __device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
 // f32x2 multiply; the add stays scalar, because the compiler contracts a packed
 // multiply feeding a packed add into a fused multiply-add whatever the rounding
 // qualifiers, and a fused result differs from the two-rounding definition.
+// With FUSED_ASM the two mixed-precision subtracts write the halves of the
+// multiply's 64-bit operand directly (one asm block, no register shuffling);
+// that form is faster at K=2 and costs registers at K=3 and K=4.
+template <bool FUSED_ASM>
 __device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, const float y,
                                           int &c0, int &c1) {
-    const float d0 = sub_h_f((unsigned short)(vw & 0xFFFFu), y);
-    const float d1 = sub_h_f((unsigned short)(vw >> 16), y);
-    const unsigned long long dd = pack2(d0, d1);
-    const unsigned long long q = mul2(dd, dd);
+    unsigned long long q;
+    if constexpr (FUSED_ASM) {
+        asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
+            "mov.b32 {hl, hh}, %1;\n\t"
+            "sub.rn.f32.f16 a, hl, %2;\n\t"
+            "sub.rn.f32.f16 b, hh, %2;\n\t"
+            "mov.b64 d, {a, b};\n\t"
+            "mul.rn.f32x2 %0, d, d;\n\t}"
+            : "=l"(q) : "r"(vw), "f"(y));
+    } else {
+        const float d0 = sub_h_f((unsigned short)(vw & 0xFFFFu), y);
+        const float d1 = sub_h_f((unsigned short)(vw >> 16), y);
+        const unsigned long long dd = pack2(d0, d1);
+        q = mul2(dd, dd);
+    }
     c0 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q & 0xffffffffull))));
     c1 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q >> 32))));
 }
 
 // Candidate k of the pair, then the running minimum (ties keep the lower k).
+template <int K>
 __device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
                                          int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
     int c0, c1;
-    cand_pair(mk, vw, y, c0, c1);
+    cand_pair<K == 2>(mk, vw, y, c0, c1);
     if (k == 0) {
         best0 = c0;
         best1 = c1;
@@ -154,7 +170,7 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
                 uint32_t bk0 = 0u, bk1 = 0u;
 #pragma unroll
                 for (int k = 0; k < Gm::NK; k++)
-                    acs_pair(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1,
+                    acs_pair<K>(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1,
                              bk0, bk1);
                 finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
             }
@@ -167,7 +183,7 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
                 const float mk = Mp[(k << (16 - 2 * K)) | hp];
 #pragma unroll
                 for (int jp = 0; jp < Gm::NJ; jp += 2)
-                    acs_pair(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best[jp],
+                    acs_pair<K>(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best[jp],
                              best[jp + 1], bk[jp], bk[jp + 1]);
             }
 #pragma unroll
