@@ -163,7 +163,7 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
             float m[Gm::NK];
 #pragma unroll
             for (int k = 0; k < Gm::NK; k++)
-                m[k] = Mp[(k << (16 - 2 * K)) | hp];
+                m[k] = Mp[(k << (16 - 2 * K)) + hp];
 #pragma unroll
             for (int jp = 0; jp < Gm::NJ; jp += 2) {
                 int best0 = 0, best1 = 0;
@@ -180,7 +180,7 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
             uint32_t bk[Gm::NJ];
 #pragma unroll
             for (int k = 0; k < Gm::NK; k++) {
-                const float mk = Mp[(k << (16 - 2 * K)) | hp];
+                const float mk = Mp[(k << (16 - 2 * K)) + hp];
 #pragma unroll
                 for (int jp = 0; jp < Gm::NJ; jp += 2)
                     acs_pair<K>(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best[jp],
@@ -192,7 +192,7 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
                                        outv, word, key);
         }
         if (!ARGMIN) {
-            float *dst = Mn + (((uint32_t)hp << K) | (uint32_t)j0);
+            float *dst = Mn + (hp << K) + j0;
 #pragma unroll
             for (int q = 0; q < Gm::NJ; q += 4)
                 *reinterpret_cast<float4 *>(dst + q) =
