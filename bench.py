@@ -47,7 +47,10 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # DRAM traffic of one encode launch per tile, from an ncu capture
 # (profiles/encode_k2_linear4096.md); valid only for the source it was taken on.
 ENCODE_TRAFFIC = {
-    # "sha256 of csrc/encode.cu": bytes per tile
+    # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
+    # `ncu --set full` on 1,216 tiles (profiles/encode_k2_small.md); the traffic is
+    # the decision rows, proportional to the tiles processed.
+    "b2fadfc8ecd3400c86055958aa46dbb2a55aeb8d8e117366d90077e056f95146": 1547184.0,
 }
 
 WORKLOAD = "linear4096_k2"
