@@ -2,10 +2,13 @@
 
     python -m exl3_trellis_weight_gb300.profile_cases encode --K 2 --rows 1216 --cols 256
     python -m exl3_trellis_weight_gb300.profile_cases rotate --rows 4096 --cols 4096
+    python -m exl3_trellis_weight_gb300.profile_cases alu-mix
 
-encode : exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1.
-rotate : exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix.
-Each case runs --reps launches and synchronises; it prints the wall time.
+encode  : exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1.
+rotate  : exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix.
+alu-mix : build and run microbench/alu_mix.cu (instruction issue rates per SM
+          per clock of the kinds the encoder uses).
+Each launch case runs --reps launches and synchronises; it prints the wall time.
 """
 from __future__ import annotations
 
@@ -25,12 +28,19 @@ def main(argv=None) -> int:
     from exl3_trellis_weight_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["encode", "rotate"])
+    ap.add_argument("case", choices=["encode", "rotate", "alu-mix"])
     ap.add_argument("--K", type=int, default=2)
     ap.add_argument("--rows", type=int, default=1216)
     ap.add_argument("--cols", type=int, default=256)
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args(argv)
+    if a.case == "alu-mix":
+        import subprocess
+        src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "microbench", "alu_mix.cu")
+        exe = os.path.join(build.BUILD, "alu_mix")
+        os.makedirs(build.BUILD, exist_ok=True)
+        subprocess.run([build.nvcc(), *build.ARCH, "-O3", src, "-o", exe], check=True)
+        return subprocess.run([exe]).returncode
     build.build()
     dev = torch.device("cuda:0")
     if a.case == "encode":
