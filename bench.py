@@ -101,24 +101,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sms, maxs, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sms.append(float(parts[0]))
-                maxs.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sms:
-            return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        return parse_clock_csv(out)
+
+
+def parse_clock_csv(text: str):
+    """Median SM clock, max clock and the throttle reasons seen in nvidia-smi CSV
+    lines (clocks.sm, clocks.max.sm, power, active mask, hw_slowdown,
+    hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap)."""
+    sms, maxs, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sms.append(float(parts[0]))
+            maxs.append(float(parts[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[4:8]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sms:
+        return None
+    return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+            "reasons": sorted(reasons), "samples": len(sms)}
 
 
 def _dist():
