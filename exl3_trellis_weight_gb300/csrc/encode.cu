@@ -99,11 +99,11 @@ __device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, con
 }
 
 // Candidate k of the pair, then the running minimum (ties keep the lower k).
-template <int K>
+template <bool FUSED_ASM>
 __device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
                                          int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
     int c0, c1;
-    cand_pair<K == 2>(mk, vw, y, c0, c1);
+    cand_pair<FUSED_ASM>(mk, vw, y, c0, c1);
     if (k == 0) {
         best0 = c0;
         best1 = c1;
@@ -138,15 +138,9 @@ __device__ __forceinline__ void finish_pair(const int u, const int jp, const int
     }
 }
 
-// One add-compare-select step over the thread's 64 candidate states.
-//   M_t(g) = min_k fl(M_{t-1}((k << (16-2K)) | (g >> K)) + fl(fl(y - v)^2)),
-// lowest k on ties.  Tracked entries are handled in pairs (jj, jj+1), which
-// share their predecessor costs.  Costs are non-negative binary32 values (or
-// +inf), whose bit patterns order like signed integers: the running minimum is
-// the DPX min-with-predicate, keeping the earlier (lower k) candidate on ties.
-// Writes the thread's decision word (K bits per entry); with ARGMIN, instead of
-// storing M_t it folds (cost, full state index) of each tracked entry into
-// `key` (lexicographic minimum).
+#ifndef EXL3_ASM_SQ
+#define EXL3_ASM_SQ(K) ((K) != 3)
+#endif
 template <int K, bool ARGMIN>
 __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__restrict__ Mn,
                                          const float y, const uint32_t (&vpk)[32], const int tid,
@@ -158,7 +152,10 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
         const int hp = Gm::unit(u, tid);
         const int j0 = Gm::j0(tid);
         float outv[Gm::NJ];
-        if (Gm::NK <= 2 * Gm::NJ) {
+#ifndef EXL3_ORDER
+#define EXL3_ORDER(K) ((K) == 4 ? 2 : 0)
+#endif
+        if constexpr (EXL3_ORDER(K) == 0) {
             // predecessor costs live (NK registers), one pair of entries at a time
             float m[Gm::NK];
 #pragma unroll
@@ -170,8 +167,21 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
                 uint32_t bk0 = 0u, bk1 = 0u;
 #pragma unroll
                 for (int k = 0; k < Gm::NK; k++)
-                    acs_pair<K>(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1,
-                             bk0, bk1);
+                    acs_pair<EXL3_ASM_SQ(K)>(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k,
+                                             best0, best1, bk0, bk1);
+                finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
+            }
+        } else if constexpr (EXL3_ORDER(K) == 2) {
+            // predecessor cost reloaded from shared memory for each pair of entries
+#pragma unroll
+            for (int jp = 0; jp < Gm::NJ; jp += 2) {
+                int best0 = 0, best1 = 0;
+                uint32_t bk0 = 0u, bk1 = 0u;
+#pragma unroll
+                for (int k = 0; k < Gm::NK; k++)
+                    acs_pair<EXL3_ASM_SQ(K)>(Mp[(k << (16 - 2 * K)) + hp],
+                                             vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k,
+                                             best0, best1, bk0, bk1);
                 finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
             }
         } else {
@@ -183,8 +193,8 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
                 const float mk = Mp[(k << (16 - 2 * K)) + hp];
 #pragma unroll
                 for (int jp = 0; jp < Gm::NJ; jp += 2)
-                    acs_pair<K>(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best[jp],
-                             best[jp + 1], bk[jp], bk[jp + 1]);
+                    acs_pair<EXL3_ASM_SQ(K)>(mk, vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k,
+                                             best[jp], best[jp + 1], bk[jp], bk[jp + 1]);
             }
 #pragma unroll
             for (int jp = 0; jp < Gm::NJ; jp += 2)
