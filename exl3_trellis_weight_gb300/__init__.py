@@ -18,6 +18,7 @@ import threading
 
 __all__ = [
     "Exl3Error", "lib", "lib_path", "rotate", "encode_tiles", "decode_tiles", "mse",
+    "encode_rows", "decode_rows",
     "quantize", "gss_scale", "encode_workspace_bytes", "encode_workspace_min_bytes",
     "quantize_workspace_bytes", "gss_workspace_bytes", "mse_workspace_bytes",
     "supports_k", "profile_enable", "profile_read", "EXL3_F32", "EXL3_BF16",
@@ -67,6 +68,8 @@ def lib():
         L.exl3_encode_workspace_min_bytes.restype = sz
         L.exl3_encode_tiles.argtypes = [P, i64, i64, i32, f32, P, P, P, sz, P]
         L.exl3_decode_tiles.argtypes = [P, i64, i64, i32, f32, P, P]
+        L.exl3_encode_rows.argtypes = [P, i64, i32, i32, f32, P, P, P, sz, P]
+        L.exl3_decode_rows.argtypes = [P, i64, i32, i32, f32, P, P]
         L.exl3_mse_workspace_bytes.argtypes = [i64, i64]
         L.exl3_mse_workspace_bytes.restype = sz
         L.exl3_mse.argtypes = [P, i32, P, i64, i64, P, P, sz, P]
@@ -80,7 +83,7 @@ def lib():
         L.exl3_profile_enable.argtypes = [i32]
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
-        for name in ("exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
+        for name in ("exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
         _lib = L
@@ -203,6 +206,34 @@ def encode_tiles(Y, K: int, scale: float = 1.0, codes=None, tile_cost=None,
                                    _ptr(tile_cost), _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(Y.device)))
     return (codes, tile_cost) if want_cost or tile_cost is not None else codes
+
+
+def encode_rows(Y, K: int, scale: float = 1.0, codes=None, row_cost=None,
+                want_cost: bool = False, ws=None):
+    """exl3_encode_rows: each row of Y[n_rows, T] is one tile -> codes uint16 [n_rows, T*K/16]."""
+    torch = _torch()
+    _need_cuda(Y, codes, row_cost)
+    n_rows, T = Y.shape
+    if codes is None:
+        codes = torch.empty(n_rows, T * K // 16, dtype=torch.int16, device=Y.device)
+    if want_cost and row_cost is None:
+        row_cost = torch.empty(n_rows, dtype=torch.float32, device=Y.device)
+    ws = _workspace(encode_workspace_bytes(n_rows, K), Y.device, ws)
+    _check(lib().exl3_encode_rows(_ptr(Y), n_rows, T, K, ctypes.c_float(scale), _ptr(codes),
+                                  _ptr(row_cost), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(Y.device)))
+    return (codes, row_cost) if want_cost or row_cost is not None else codes
+
+
+def decode_rows(codes, n_rows: int, T: int, K: int, scale: float = 1.0, out=None):
+    """exl3_decode_rows -> fp32 [n_rows, T]."""
+    torch = _torch()
+    _need_cuda(codes, out)
+    if out is None:
+        out = torch.empty(n_rows, T, dtype=torch.float32, device=codes.device)
+    _check(lib().exl3_decode_rows(_ptr(codes), n_rows, T, K, ctypes.c_float(scale), _ptr(out),
+                                  _stream(codes.device)))
+    return out
 
 
 def decode_tiles(codes, rows: int, cols: int, K: int, scale: float = 1.0, out=None):

@@ -326,6 +326,8 @@ exl3_status run_quantize(const QuantWs &q, int grid, const void *W, int dt, int6
     el.rows = rows;
     el.cols = cols;
     el.K = K;
+    el.T = 256;
+    el.row_tiles = 0;
     el.inv_scale = 1.0f;
     el.inv_scale_dev = &q.fscal[1];
     el.codes = codes;
@@ -443,6 +445,8 @@ exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K,
     el.rows = rows;
     el.cols = cols;
     el.K = K;
+    el.T = 256;
+    el.row_tiles = 0;
     el.inv_scale = 1.0f / scale;   // IEEE binary32 division, round to nearest
     el.inv_scale_dev = nullptr;
     el.codes = reinterpret_cast<uint32_t *>(codes);
@@ -450,6 +454,64 @@ exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K,
     el.scratch = reinterpret_cast<uint32_t *>(ws);
     el.grid = (int)grid;
     return launch_encode(el, (cudaStream_t)stream);
+}
+
+static exl3_status check_rows(int64_t n_rows, int T, int K) {
+    exl3_status st;
+    if ((st = check_k(K)) != EXL3_OK) return st;
+    if (n_rows <= 0 || n_rows > (1ll << 26))
+        return set_error(EXL3_ERR_INVALID_ARG, "n_rows=%lld outside [1, 2^26]", (long long)n_rows);
+    if (T < 16 || T > 256 || (T & 1) || (T * K) % 32)
+        return set_error(EXL3_ERR_UNSUPPORTED,
+                         "T=%d: need an even T in [16, 256] with T*K a multiple of 32 (K=%d)", T, K);
+    return EXL3_OK;
+}
+
+exl3_status exl3_encode_rows(const float *Y, int64_t n_rows, int T, int K, float scale,
+                             uint16_t *codes, float *row_cost, void *ws, size_t ws_bytes,
+                             void *stream) {
+    exl3_status st;
+    if ((st = check_rows(n_rows, T, K)) != EXL3_OK) return st;
+    if ((st = check_ptr(Y, "Y", 4)) != EXL3_OK) return st;
+    if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
+    if (row_cost && !aligned(row_cost, 4))
+        return set_error(EXL3_ERR_INVALID_ARG, "row_cost is not 4-byte aligned");
+    if (!(scale > 0.0f) || !std::isfinite(scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (!ws || !aligned(ws, kAlign))
+        return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    const int64_t cap = (int64_t)(ws_bytes / kEncodeBlockScratchBytes);
+    if (cap < 1)
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes < minimum %zu", ws_bytes,
+                         kEncodeBlockScratchBytes);
+    int64_t grid = encode_grid_full(n_rows);
+    if (grid > cap) grid = cap;
+    EncodeLaunch el{};
+    el.Y = Y;
+    el.rows = n_rows;
+    el.cols = T;
+    el.K = K;
+    el.T = T;
+    el.row_tiles = 1;
+    el.inv_scale = 1.0f / scale;
+    el.inv_scale_dev = nullptr;
+    el.codes = reinterpret_cast<uint32_t *>(codes);
+    el.tile_cost = row_cost;
+    el.scratch = reinterpret_cast<uint32_t *>(ws);
+    el.grid = (int)grid;
+    return launch_encode(el, (cudaStream_t)stream);
+}
+
+exl3_status exl3_decode_rows(const uint16_t *codes, int64_t n_rows, int T, int K, float scale,
+                             float *Yhat, void *stream) {
+    exl3_status st;
+    if ((st = check_rows(n_rows, T, K)) != EXL3_OK) return st;
+    if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
+    if ((st = check_ptr(Yhat, "Yhat", 4)) != EXL3_OK) return st;
+    if (!std::isfinite(scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale must be finite");
+    return launch_decode_rows(reinterpret_cast<const uint32_t *>(codes), n_rows, T, K, scale, Yhat,
+                              (cudaStream_t)stream);
 }
 
 exl3_status exl3_decode_tiles(const uint16_t *codes, int64_t rows, int64_t cols, int K, float scale,

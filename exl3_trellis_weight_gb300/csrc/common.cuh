@@ -115,6 +115,8 @@ struct EncodeLaunch {
     const float *Y;
     int64_t rows, cols;
     int K;
+    int T;                       // steps per tile (256 for 16x16 tiles)
+    int row_tiles;               // 0: 16x16 tiles of Y[rows, cols]; 1: each row of Y[rows, T] is a tile
     float inv_scale;             // used when inv_scale_dev == nullptr
     const float *inv_scale_dev;  // device scalar or nullptr
     uint32_t *codes;             // [n_tiles][8K] uint32
@@ -128,6 +130,8 @@ exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s);
 
 exl3_status launch_decode(const uint32_t *codes, int64_t rows, int64_t cols, int K,
                           float scale, const float *scale_dev, float *out, cudaStream_t s);
+exl3_status launch_decode_rows(const uint32_t *codes, int64_t n_rows, int T, int K, float scale,
+                               float *out, cudaStream_t s);
 
 // rotation modes
 enum RotSrc { SRC_F32 = 0, SRC_BF16 = 1, SRC_CODES = 2 };

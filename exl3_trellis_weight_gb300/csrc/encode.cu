@@ -1,14 +1,16 @@
 // encode.cu -- persistent trellis tile encoder (page "EXL3 Intel Arc
 // Quantizer", Core Implemented Architecture items 1, 4 and 5).
 //
-// One 1024-thread block per SM walks its share of the tiles.  For each tile:
-//   pass 1: targets rolled left by 128, free start, 256 add-compare-select
-//           steps; decisions of steps 127..254 are kept; the lowest-index
-//           minimal final state is traced back to step 127 -> end_state.
-//   pass 2: unrolled targets, first predecessor fixed to end_state, 255 steps
-//           (step 255 of the constrained pass is never needed: its path is
-//           forced to end at end_state); traced back from end_state; the low
-//           K bits of each state are packed MSB first.
+// One 1024-thread block per SM walks its share of the tiles.  A tile is T
+// targets: the 256 elements of a 16x16 tile (row-major), or one row of T
+// elements (even T in [16, 256]).  For each tile:
+//   pass 1: targets rolled left by T/2, free start, T add-compare-select
+//           steps; decisions of steps T/2-1..T-2 are kept; the lowest-index
+//           minimal final state is traced back to step T/2-1 -> end_state.
+//   pass 2: unrolled targets, first predecessor fixed to end_state, T-1 steps
+//           (the last step of the constrained pass is never needed: its path
+//           is forced to end at end_state); traced back from end_state; the
+//           low K bits of each state are packed MSB first.
 //
 // The tracked cost row M (2^(16-K) fp32) is double-buffered in shared memory;
 // the mul1 level of each of a thread's 64 candidate states is fixed for the
@@ -242,13 +244,15 @@ __device__ __forceinline__ void tb_advance(Tb &tb, uint32_t *bs) {
         tb.on = false;
 }
 
-template <int K>
+// TT: tile length fixed at compile time (256 for 16x16 tiles) or 0 (rows of
+// a.T targets).
+template <int K, int TT>
 __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch a) {
     using Gm = Geo<K>;
     extern __shared__ __align__(16) unsigned char smem[];
     float *M0 = reinterpret_cast<float *>(smem);
     float *M1 = M0 + Gm::G;
-    float *ys = M1 + Gm::G;                                       // 256 targets
+    float *ys = M1 + Gm::G;                                       // up to 256 targets
     uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);         // packed codes (tb2)
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
     __shared__ uint32_t sh_sstar[2], sh_end[2];
@@ -273,8 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
 
     const float inv_s = a.inv_scale_dev ? __ldg(a.inv_scale_dev) : a.inv_scale;
     // tile bookkeeping fits 32 bits: the ABI bounds a matrix to 2^34 elements
-    const int tiles_c = (int)(a.cols / 16);
-    const int n_tiles = (int)(a.rows / 16) * tiles_c;
+    const int T = TT ? TT : a.T;       // even, 16..256
+    const int half = T / 2;
+    const int code_words = T * K / 32;
+    const bool row_tiles = TT == 0;
+    const int tiles_c = row_tiles ? 1 : (int)(a.cols / 16);
+    const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
     const int grid = (int)gridDim.x;
     const int n_my = n_tiles > (int)blockIdx.x ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
     // decision buffers of this block: pass-1 slots 0/1, then pass-2 slots 0/1
@@ -318,10 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
         const int f_tile = (int)blockIdx.x + f_loc * grid;
 
         if (fwd) {
-            const int tr = f_tile / tiles_c, tc = f_tile % tiles_c;
-            if (tid < 256) {
-                const int i = (f_pass == 1) ? ((tid + 128) & 255) : tid;
-                const float *src = a.Y + (size_t)(tr * 16 + (i >> 4)) * (size_t)a.cols + tc * 16 + (i & 15);
+            if (tid < T) {
+                const int i = (f_pass == 1) ? (tid + half < T ? tid + half : tid + half - T) : tid;
+                const float *src;
+                if (row_tiles) {
+                    src = a.Y + (size_t)f_tile * (size_t)T + i;
+                } else {
+                    const int tr = f_tile / tiles_c, tc = f_tile % tiles_c;
+                    src = a.Y + (size_t)(tr * 16 + (i >> 4)) * (size_t)a.cols + tc * 16 + (i & 15);
+                }
                 ys[tid] = __fmul_rn(__ldg(src), inv_s);
             }
             if (f_pass == 1) {
@@ -338,20 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
             tb.pass = b_pass;
             tb.slot = b_slot;
             tb.tile = (int)blockIdx.x + b_loc * grid;
-            tb.t = 255;
+            tb.t = T - 1;
             if (b_pass == 1) {
                 tb.s = sh_sstar[b_slot];
-                tb.stop = 127;
+                tb.stop = half - 1;
                 tb.rows = scr + (size_t)b_slot * kP1;
-                tb.row0 = 127;
+                tb.row0 = half - 1;
             } else {
                 tb.s = sh_end[b_slot];
                 tb.stop = 0;
                 tb.rows = scr + 2 * kP1 + (size_t)b_slot * kP2;
                 tb.row0 = 0;
-                for (int w = 0; w < 8 * K; w++)
+                for (int w = 0; w < code_words; w++)
                     bs[w] = 0u;
-                put_code<K>(bs, 255, tb.s & (uint32_t)(Gm::NK - 1));
+                put_code<K>(bs, T - 1, tb.s & (uint32_t)(Gm::NK - 1));
             }
         }
         __syncthreads();
@@ -359,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
         if (fwd) {
             uint32_t *rows = (f_pass == 1) ? scr + (size_t)f_slot * kP1
                                            : scr + 2 * kP1 + (size_t)f_slot * kP2;
-            const int row0 = (f_pass == 1) ? 127 : 0;
-            for (int t = 0; t < 255; t++) {
+            const int row0 = (f_pass == 1) ? half - 1 : 0;
+            for (int t = 0; t < T - 1; t++) {
                 if (tid == 0 && tb.on)
                     tb_issue<K>(tb);
                 const float *Mp = (t & 1) ? M1 : M0;
@@ -375,12 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 __syncthreads();
             }
             if (f_pass == 1) {
-                // step 255 (reads M_254 from M1): lowest full state with minimal cost
+                // step T-1 (T even: reads M_{T-2} from M1): lowest full state with minimal cost
                 if (tid == 0 && tb.on)
                     tb_issue<K>(tb);
                 uint32_t word;
                 unsigned long long key = ~0ull;
-                acs_step<K, true>(M1, nullptr, ys[255], vpk, tid, word, key);
+                acs_step<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
                 if (tid == 0 && tb.on)
                     tb_advance<K>(tb, bs);
                 key = warp_min_u64(key);
@@ -393,9 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                         sh_sstar[f_slot] = (uint32_t)(key & 0xffffffffull);
                 }
             } else if (tid == 0 && a.tile_cost) {
-                // path forced to end at end_state: fl(M_254(end >> K) + q_255(end))
+                // path forced to end at end_state: fl(M_{T-2}(end >> K) + q_{T-1}(end))
                 const uint32_t e = sh_end[f_slot];
-                const float d = __fsub_rn(ys[255], mul1_value(e));
+                const float d = __fsub_rn(ys[T - 1], mul1_value(e));
                 a.tile_cost[f_tile] = __fadd_rn(M1[e >> K], __fmul_rn(d, d));
             }
         }
@@ -407,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
             if (tb.pass == 1) {
                 sh_end[tb.slot] = tb.s;
             } else {
-                uint32_t *dst = a.codes + (size_t)tb.tile * (8 * K);
-                for (int w = 0; w < 8 * K; w++)
+                uint32_t *dst = a.codes + (size_t)tb.tile * code_words;
+                for (int w = 0; w < code_words; w++)
                     dst[w] = bs[w];
             }
         }
@@ -416,49 +429,47 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     }
 }
 
-template <int K>
-exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s) {
+template <int K, int TT>
+exl3_status launch_kt(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
     const size_t smem = (size_t)(2 * Gm::G + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
-    cudaError_t e = cudaFuncSetAttribute(encode_kernel<K>,
+    cudaError_t e = cudaFuncSetAttribute(encode_kernel<K, TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_check(e, "cudaFuncSetAttribute(encode)");
-    profile_encode_begin(s);
-    encode_kernel<K><<<p.grid, kThreads, smem, s>>>(p);
-    note_launch();
-    profile_encode_end(s);
+    if (profiled)
+        profile_encode_begin(s);
+    encode_kernel<K, TT><<<p.grid, kThreads, smem, s>>>(p);
+    if (profiled) {
+        note_launch();
+        profile_encode_end(s);
+    }
     return cuda_check(cudaGetLastError(), "encode launch");
 }
 
 template <int K>
-exl3_status launch_k_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
-    using Gm = Geo<K>;
-    const size_t smem = (size_t)(2 * Gm::G + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
-    cudaError_t e = cudaFuncSetAttribute(encode_kernel<K>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return cuda_check(e, "cudaFuncSetAttribute(encode)");
-    encode_kernel<K><<<p.grid, kThreads, smem, s>>>(p);
-    return cuda_check(cudaGetLastError(), "encode launch");
+exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    if (p.row_tiles)
+        return launch_kt<K, 0>(p, s, profiled);
+    return launch_kt<K, 256>(p, s, profiled);
 }
 
 }  // namespace
 
 exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
     switch (p.K) {
-    case 2: return launch_k_unprofiled<2>(p, s);
-    case 3: return launch_k_unprofiled<3>(p, s);
-    case 4: return launch_k_unprofiled<4>(p, s);
+    case 2: return launch_k<2>(p, s, false);
+    case 3: return launch_k<3>(p, s, false);
+    case 4: return launch_k<4>(p, s, false);
     default: return set_error(EXL3_ERR_UNSUPPORTED, "K=%d is not built", p.K);
     }
 }
 
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s) {
     switch (p.K) {
-    case 2: return launch_k<2>(p, s);
-    case 3: return launch_k<3>(p, s);
-    case 4: return launch_k<4>(p, s);
+    case 2: return launch_k<2>(p, s, true);
+    case 3: return launch_k<3>(p, s, true);
+    case 4: return launch_k<4>(p, s, true);
     default: return set_error(EXL3_ERR_UNSUPPORTED, "K=%d is not built", p.K);
     }
 }

@@ -94,6 +94,8 @@ extern "C" EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_
     el.rows = rows;
     el.cols = cols;
     el.K = K;
+    el.T = 256;
+    el.row_tiles = 0;
     el.inv_scale = 1.0f / scale;
     el.inv_scale_dev = nullptr;
     el.codes = reinterpret_cast<uint32_t *>(codes);

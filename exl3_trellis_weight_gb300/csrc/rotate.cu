@@ -234,6 +234,27 @@ __global__ void __launch_bounds__(128) decode_kernel(const uint32_t *__restrict_
     }
 }
 
+// Rows of T targets: one thread per element; state i is the 16-bit window of
+// the row's circular T*K-bit stream ending with the last bit of code i.
+__global__ void decode_rows_kernel(const uint32_t *__restrict__ codes, int64_t n_rows, int T, int K,
+                                   float scale, float *__restrict__ out) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n_rows * T)
+        return;
+    const int64_t r = e / T;
+    const int i = (int)(e % T);
+    const int NB = T * K, NW = T * K / 32;
+    const uint32_t *w = codes + (size_t)r * NW;
+    int p = (i + 1) * K - 16;
+    while (p < 0)
+        p += NB;
+    const int wi = p >> 5;
+    const int wj = (wi + 1 == NW) ? 0 : wi + 1;
+    const unsigned long long cat = ((unsigned long long)__ldg(w + wi) << 32) | __ldg(w + wj);
+    const uint32_t st = (uint32_t)(cat >> (48 - (p & 31))) & 0xFFFFu;
+    out[e] = __fmul_rn(mul1_value(st), scale);
+}
+
 // Per-tile fp64 sum of x^2 or (x - ref)^2, one thread per tile.
 __global__ void tile_sumsq_kernel(const void *x, int x_dt, const float *ref, int64_t rows,
                                   int64_t cols, double *out) {
@@ -313,6 +334,16 @@ exl3_status launch_decode(const uint32_t *codes, int64_t rows, int64_t cols, int
     decode_kernel<<<(unsigned)nblk, 128, 0, s>>>(codes, rows, cols, K, scale, scale_dev, out);
     note_launch();
     return cuda_check(cudaGetLastError(), "decode launch");
+}
+
+exl3_status launch_decode_rows(const uint32_t *codes, int64_t n_rows, int T, int K, float scale,
+                               float *out, cudaStream_t s) {
+    const int64_t n = n_rows * T;
+    if (n == 0)
+        return EXL3_OK;
+    decode_rows_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(codes, n_rows, T, K, scale, out);
+    note_launch();
+    return cuda_check(cudaGetLastError(), "decode_rows launch");
 }
 
 exl3_status launch_tile_sumsq(const void *x, int x_dt, const float *ref, int64_t rows, int64_t cols,

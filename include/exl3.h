@@ -140,6 +140,24 @@ EXL3_API exl3_status exl3_decode_tiles(const uint16_t *codes, int64_t rows, int6
                               float scale, float *Yhat, void *stream);
 
 /*
+ * Row-wise variants for tiles that are not 16x16: every row of Y[n_rows, T]
+ * is one tile of T targets (README item 1: "standard L=256 tiles, and L=160
+ * n-gram rows").  Same two-pass search, codebook and packing as
+ * exl3_encode_tiles, with the pass-1 roll T/2 and a T*K-bit circular stream
+ * per row stored as T*K/16 uint16 words (MSB first, SWAP16).
+ *   T even, 16 <= T <= 256, (T*K) % 32 == 0 (e.g. T = 160 for K = 2, 3, 4).
+ *   codes (device, 4-byte aligned) uint16 [n_rows][T*K/16];
+ *   row_cost (device) fp32 [n_rows] or NULL.
+ *   ws: exl3_encode_workspace_bytes(n_rows, K) (same per-block scratch).
+ * exl3_decode_rows writes Yhat[n_rows, T] = fl(v(state) * scale).
+ */
+EXL3_API exl3_status exl3_encode_rows(const float *Y, int64_t n_rows, int T, int K, float scale,
+                                      uint16_t *codes, float *row_cost, void *ws, size_t ws_bytes,
+                                      void *stream);
+EXL3_API exl3_status exl3_decode_rows(const uint16_t *codes, int64_t n_rows, int T, int K,
+                                      float scale, float *Yhat, void *stream);
+
+/*
  * Reconstruction MSE (README item 10): sum over tiles of the fp64 squared
  * error sum((double)W - (double)What)^2, each tile summed sequentially in
  * row-major order and the tile sums added as a pairwise tree (neighbours

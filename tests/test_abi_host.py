@@ -119,3 +119,19 @@ def test_workspace_queries_scale_with_work(ex):
     assert ex.encode_workspace_bytes(100, 1) == 0
     assert ex.quantize_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
     assert ex.gss_workspace_bytes(4096, 4096, 2) > ex.quantize_workspace_bytes(4096, 4096, 2)
+
+
+def test_rows_reject_bad_lengths(ex):
+    L = ex.lib()
+    ws_min = ex.encode_workspace_min_bytes(2)
+    enc = lambda n, T, K, ws=ws_min: L.exl3_encode_rows(FAKE, n, T, K, ctypes.c_float(1.0), FAKE,
+                                                        None, FAKE, ws, None)
+    assert enc(10, 161, 2) == 2          # odd T
+    assert enc(10, 258, 2) == 2          # T > 256
+    assert enc(10, 8, 4) == 2            # T < 16
+    assert enc(10, 48, 3) == 2           # T*K not a multiple of 32
+    assert enc(0, 160, 2) == 1
+    assert enc(10, 160, 5) == 2
+    assert enc(10, 160, 2, ws=ws_min - 1) == 3
+    dec = lambda n, T, K: L.exl3_decode_rows(FAKE, n, T, K, ctypes.c_float(1.0), FAKE, None)
+    assert dec(10, 161, 2) == 2 and dec(-1, 160, 2) == 1

@@ -332,3 +332,47 @@ def test_profile_counts_launches(ex):
     ex.profile_enable(False)
     assert n_enc == 1 and ms > 0
     assert n_all >= 7
+
+
+# ---------------------------------------------------------------------------
+# rows of T targets (non-256 tile lengths)
+# ---------------------------------------------------------------------------
+
+ROW_CASES = [(160, 2), (160, 3), (160, 4), (16, 2), (48, 2), (96, 3), (64, 4), (256, 2), (32, 4)]
+
+
+@pytest.mark.parametrize("T,K", ROW_CASES)
+def test_encode_rows_bit_exact(ex, T, K):
+    rng = np.random.default_rng(T * 10 + K)
+    n_rows = 37
+    Y = rng.standard_normal((n_rows, T)).astype(np.float32)
+    codes, cost = ex.encode_rows(torch.from_numpy(Y).to(DEV), K, 1.3, want_cost=True)
+    torch.cuda.synchronize()
+    inv = np.float32(1.0) / np.float32(1.3)
+    got = codes.cpu().numpy().view(np.uint16)
+    for r in range(n_rows):
+        st, c, _ = oracle.encode_tile((Y[r] * inv).astype(np.float32), K)
+        assert np.array_equal(got[r], oracle.pack(st, K)), (T, K, r)
+    want_cost = np.array([oracle.encode_tile((Y[r] * inv).astype(np.float32), K)[1]
+                          for r in range(n_rows)], dtype=np.float32)
+    assert np.array_equal(cost.cpu().numpy().view(np.uint32), want_cost.view(np.uint32))
+    # decode through the library matches the oracle's decode of the same words
+    dec = ex.decode_rows(codes, n_rows, T, K, 1.3)
+    torch.cuda.synchronize()
+    want = np.stack([oracle.decode_values(oracle.unpack_states(got[r], K, T=T), 1.3)
+                     for r in range(n_rows)])
+    assert np.array_equal(dec.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+def test_encode_rows_one_block_many_rows(ex):
+    """All rows through one persistent block: odd count, pipeline drain."""
+    T, K, n_rows = 160, 2, 9
+    rng = np.random.default_rng(77)
+    Y = rng.standard_normal((n_rows, T)).astype(np.float32)
+    ws = torch.empty(ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
+    codes = ex.encode_rows(torch.from_numpy(Y).to(DEV), K, 1.0, ws=ws)
+    torch.cuda.synchronize()
+    got = codes.cpu().numpy().view(np.uint16)
+    for r in range(n_rows):
+        st, _, _ = oracle.encode_tile(Y[r], K)
+        assert np.array_equal(got[r], oracle.pack(st, K))
