@@ -99,7 +99,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-bool k_ok(int K) { return K >= 2 && K <= 4; }
+bool k_ok(int K) { return K >= 1 && K <= 4; }
 
 size_t dt_size(int dt) { return dt == EXL3_BF16 ? 2 : 4; }
 
@@ -115,9 +115,24 @@ struct Carver {
     }
 };
 
-int encode_grid_full(int64_t n_tiles) {
+// Persistent blocks for the whole machine.  K = 1 runs two-block clusters
+// (one tile per cluster at a time), so its grid is even.
+int encode_grid_full(int64_t n_tiles, int K) {
     const int64_t sm = device_sm_count();
+    if (K == 1) {
+        const int64_t g = 2 * n_tiles;
+        const int64_t smax = sm & ~1ll;
+        return (int)(g < smax ? g : smax);
+    }
     return (int)(n_tiles < sm ? n_tiles : sm);
+}
+
+// Grid that fits `cap` block slices (even for K = 1); 0 if none fits.
+int64_t fit_blocks(int64_t full, int64_t cap, int K) {
+    int64_t g = full < cap ? full : cap;
+    if (K == 1)
+        g &= ~1ll;
+    return g;
 }
 
 struct QuantWs {
@@ -285,7 +300,7 @@ exl3_status check_signs(const float *su, const float *sv) {
 
 exl3_status check_k(int K) {
     if (!k_ok(K))
-        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: this build encodes K in {2,3,4}", K);
+        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: this build encodes K in {1,2,3,4}", K);
     return EXL3_OK;
 }
 
@@ -412,12 +427,12 @@ exl3_status exl3_rotate(const void *W, int dt, int64_t rows, int64_t cols, const
 size_t exl3_encode_workspace_bytes(int64_t n_tiles, int K) {
     if (!k_ok(K) || n_tiles < 0)
         return 0;
-    const int64_t g = encode_grid_full(n_tiles);
-    return (size_t)(g > 0 ? g : 1) * kEncodeBlockScratchBytes;
+    const int64_t g = encode_grid_full(n_tiles, K);
+    return (size_t)(g > 0 ? g : (K == 1 ? 2 : 1)) * kEncodeBlockScratchBytes;
 }
 
 size_t exl3_encode_workspace_min_bytes(int K) {
-    return k_ok(K) ? kEncodeBlockScratchBytes : 0;
+    return k_ok(K) ? (size_t)(K == 1 ? 2 : 1) * kEncodeBlockScratchBytes : 0;
 }
 
 exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K, float scale,
@@ -434,12 +449,11 @@ exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K,
     if (!ws || !aligned(ws, kAlign))
         return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
     const int64_t n_tiles = (rows / 16) * (cols / 16);
-    const int64_t cap = (int64_t)(ws_bytes / kEncodeBlockScratchBytes);
-    if (cap < 1)
+    const int64_t grid = fit_blocks(encode_grid_full(n_tiles, K),
+                                    (int64_t)(ws_bytes / kEncodeBlockScratchBytes), K);
+    if (grid < 1)
         return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes < minimum %zu", ws_bytes,
-                         kEncodeBlockScratchBytes);
-    int64_t grid = encode_grid_full(n_tiles);
-    if (grid > cap) grid = cap;
+                         exl3_encode_workspace_min_bytes(K));
     EncodeLaunch el{};
     el.Y = Y;
     el.rows = rows;
@@ -480,12 +494,11 @@ exl3_status exl3_encode_rows(const float *Y, int64_t n_rows, int T, int K, float
         return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
     if (!ws || !aligned(ws, kAlign))
         return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
-    const int64_t cap = (int64_t)(ws_bytes / kEncodeBlockScratchBytes);
-    if (cap < 1)
+    const int64_t grid = fit_blocks(encode_grid_full(n_rows, K),
+                                    (int64_t)(ws_bytes / kEncodeBlockScratchBytes), K);
+    if (grid < 1)
         return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes < minimum %zu", ws_bytes,
-                         kEncodeBlockScratchBytes);
-    int64_t grid = encode_grid_full(n_rows);
-    if (grid > cap) grid = cap;
+                         exl3_encode_workspace_min_bytes(K));
     EncodeLaunch el{};
     el.Y = Y;
     el.rows = n_rows;
@@ -560,7 +573,7 @@ exl3_status exl3_mse(const void *W, int dt, const float *What, int64_t rows, int
 size_t exl3_quantize_workspace_bytes(int64_t rows, int64_t cols, int K) {
     if (!k_ok(K) || rows <= 0 || cols <= 0) return 0;
     const int64_t n_tiles = (rows / 16) * (cols / 16);
-    return carve_quant(nullptr, rows, cols, K, false, encode_grid_full(n_tiles)).total;
+    return carve_quant(nullptr, rows, cols, K, false, encode_grid_full(n_tiles, K)).total;
 }
 
 static exl3_status quant_common_checks(const void *W, int dt, int64_t rows, int64_t cols,
@@ -574,13 +587,13 @@ static exl3_status quant_common_checks(const void *W, int dt, int64_t rows, int6
 // grid that fits the workspace (returns 0 when even one block does not fit)
 static int fit_grid(void *ws, size_t ws_bytes, int64_t rows, int64_t cols, int K, bool gss) {
     const int64_t n_tiles = (rows / 16) * (cols / 16);
-    int g = encode_grid_full(n_tiles);
+    int g = encode_grid_full(n_tiles, K);
     const size_t fixed = carve_quant(nullptr, rows, cols, K, gss, 0).total;
     if (ws_bytes < fixed + kEncodeBlockScratchBytes)
         return 0;
     const int64_t cap = (int64_t)((ws_bytes - fixed) / kEncodeBlockScratchBytes);
     (void)ws;
-    return (int)(g < cap ? g : cap);
+    return (int)fit_blocks(g, cap, K);
 }
 
 exl3_status exl3_quantize(const void *W, int dt, int64_t rows, int64_t cols, const float *su,
@@ -612,7 +625,7 @@ exl3_status exl3_quantize(const void *W, int dt, int64_t rows, int64_t cols, con
 size_t exl3_gss_workspace_bytes(int64_t rows, int64_t cols, int K) {
     if (!k_ok(K) || rows <= 0 || cols <= 0) return 0;
     const int64_t n_tiles = (rows / 16) * (cols / 16);
-    return carve_quant(nullptr, rows, cols, K, true, encode_grid_full(n_tiles)).total;
+    return carve_quant(nullptr, rows, cols, K, true, encode_grid_full(n_tiles, K)).total;
 }
 
 exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t cols, const float *su,

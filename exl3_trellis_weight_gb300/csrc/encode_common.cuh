@@ -1,0 +1,131 @@
+// encode_common.cuh -- device helpers shared by the trellis encode kernels
+// (encode.cu: one block per tile; encode_k1.cu: a two-block cluster per tile).
+#pragma once
+
+#include "common.cuh"
+
+namespace exl3 {
+namespace {
+
+
+template <int K>
+__device__ __forceinline__ void put_code(uint32_t *bs, int t, uint32_t e) {
+    const int p = t * K;
+    const int w = p >> 5;
+    const int sh = 32 - K - (p & 31);
+    if (sh >= 0) {
+        bs[w] |= e << sh;
+    } else {
+        bs[w] |= e >> (-sh);
+        bs[w + 1] |= e << (32 + sh);
+    }
+}
+
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w < v ? w : v;
+    }
+    return v;
+}
+
+// fl(v - y) with v an fp16 value held in 16 bits (one mixed-precision subtract;
+// exact widening of v, one binary32 rounding).  (v - y)^2 == (y - v)^2 bitwise.
+__device__ __forceinline__ float sub_h_f(unsigned short v, float y) {
+    float r;
+    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(v), "f"(y));
+    return r;
+}
+
+// Two independent binary32 multiplies in one instruction.
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+
+// Candidate k of a pair of tracked entries (jj, jj+1) sharing predecessor cost
+// mk: c = fl(mk + fl(fl(v - y)^2)) for both.  The square of the pair runs as one
+// f32x2 multiply; the add stays scalar, because the compiler contracts a packed
+// multiply feeding a packed add into a fused multiply-add whatever the rounding
+// qualifiers, and a fused result differs from the two-rounding definition.
+// With FUSED_ASM the two mixed-precision subtracts write the halves of the
+// multiply's 64-bit operand directly (one asm block, no register shuffling);
+// that form is faster at K=2 and costs registers at K=3 and K=4.
+template <bool FUSED_ASM>
+__device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, const float y,
+                                          int &c0, int &c1) {
+    unsigned long long q;
+    if constexpr (FUSED_ASM) {
+        asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
+            "mov.b32 {hl, hh}, %1;\n\t"
+            "sub.rn.f32.f16 a, hl, %2;\n\t"
+            "sub.rn.f32.f16 b, hh, %2;\n\t"
+            "mov.b64 d, {a, b};\n\t"
+            "mul.rn.f32x2 %0, d, d;\n\t}"
+            : "=l"(q) : "r"(vw), "f"(y));
+    } else {
+        const float d0 = sub_h_f((unsigned short)(vw & 0xFFFFu), y);
+        const float d1 = sub_h_f((unsigned short)(vw >> 16), y);
+        const unsigned long long dd = pack2(d0, d1);
+        q = mul2(dd, dd);
+    }
+    c0 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q & 0xffffffffull))));
+    c1 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q >> 32))));
+}
+
+// Candidate k of the pair, then the running minimum (ties keep the lower k).
+template <bool FUSED_ASM>
+__device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
+                                         int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
+    int c0, c1;
+    cand_pair<FUSED_ASM>(mk, vw, y, c0, c1);
+    if (k == 0) {
+        best0 = c0;
+        best1 = c1;
+        bk0 = 0u;
+        bk1 = 0u;
+    } else {
+        bool keep0, keep1;
+        best0 = __vibmin_s32(best0, c0, &keep0);   // keep0: best0 <= c0
+        best1 = __vibmin_s32(best1, c1, &keep1);
+        bk0 = keep0 ? bk0 : (uint32_t)k;
+        bk1 = keep1 ? bk1 : (uint32_t)k;
+    }
+}
+
+template <int K, bool ARGMIN>
+__device__ __forceinline__ void finish_pair(const int u, const int jp, const int hp, const int j0,
+                                            const int best0, const int best1, const uint32_t bk0,
+                                            const uint32_t bk1, float *outv, uint32_t &word,
+                                            unsigned long long &key) {
+    using Gm = Geo<K>;
+    outv[jp] = __int_as_float(best0);
+    outv[jp + 1] = __int_as_float(best1);
+    word |= (bk0 << ((u * Gm::NJ + jp) * K)) | (bk1 << ((u * Gm::NJ + jp + 1) * K));
+    if (ARGMIN) {
+        const uint32_t g0 = ((uint32_t)hp << K) | (uint32_t)(j0 + jp);
+        const unsigned long long k0 =
+            ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << Gm::KR) | g0);
+        const unsigned long long k1 =
+            ((unsigned long long)(uint32_t)best1 << 32) | ((bk1 << Gm::KR) | (g0 + 1u));
+        key = k0 < key ? k0 : key;
+        key = k1 < key ? k1 : key;
+    }
+}
+
+struct Tb {          // traceback state, kept in shared memory, used by thread 0 only
+    const uint32_t *rows;
+    int tile;
+    uint32_t s;       // full state at step t
+    uint32_t pending; // decision word in flight
+    int t, stop, row0, pass, slot;
+    bool on;
+};
+
+}  // namespace
+}  // namespace exl3

@@ -1,0 +1,348 @@
+// encode_k1.cu -- trellis tile encoder at K = 1 bit per weight (page "EXL3 Intel
+// Arc Quantizer", Core Implemented Architecture items 1, 4 and 5: K in {1..4}).
+//
+// At K = 1 the tracked cost row has 2^15 fp32 entries (128 KiB); two copies do
+// not fit one SM's shared memory.  A tile is therefore encoded by a cluster of
+// two 1024-thread blocks on two SMs.  Block r of the cluster holds the half of
+// the row whose top index bit is r, double-buffered in its shared memory:
+//   unit h' (tracked entries 2h', 2h'+1) reads M(h') and M(16384 + h'): one cost
+//   in each half (ld.shared::cluster for the peer's, a plain load for its own)
+//   and writes M(2h'), M(2h'+1), which lie in the half of block h' >> 13.
+// Block r handles the 8192 units h' = r*8192 + u*1024 + tid (u = 0..7), so all
+// of its writes are local.  One cluster barrier separates consecutive steps.
+//
+// Everything else follows encode.cu: the same two passes, tie rules, packing,
+// 1024-word decision rows (each block writes the rows of its own entries into
+// its own workspace slice: word tid, bit 2u + j), and the same two-tile
+// pipeline with an interleaved traceback run by thread 0 of block 0.
+#include <cooperative_groups.h>
+
+#include "encode_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kHalfK1 = 16384;   // tracked entries per block
+constexpr size_t kBlockWords = kEncodeBlockScratchBytes / sizeof(uint32_t);
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Where D_t(g) of tracked entry g (15 bits) lives: owner block, word, bit.
+__device__ __forceinline__ void k1_locate(uint32_t g, int &owner, int &word, int &bit) {
+    const uint32_t hp = g >> 1;
+    owner = (int)(hp >> 13);
+    word = (int)(hp & 1023u);
+    bit = (int)(((hp >> 10) & 7u) * 2u + (g & 1u));
+}
+
+// traceback step helpers (thread 0 of block 0); tb.rows = slot rows in block 0's slice
+__device__ __forceinline__ void k1_tb_issue(Tb &tb) {
+    int owner, w, b;
+    k1_locate(tb.s >> 1, owner, w, b);
+    tb.pending = __ldcg(tb.rows + (size_t)owner * kBlockWords +
+                        (size_t)(tb.t - 1 - tb.row0) * kRowWords + w);
+}
+
+__device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
+    const uint32_t g = tb.s >> 1;
+    int owner, w, b;
+    k1_locate(g, owner, w, b);
+    const uint32_t k = (tb.pending >> b) & 1u;
+    tb.s = (k << 15) | g;
+    tb.t -= 1;
+    if (tb.pass == 2)
+        put_code<1>(bs, tb.t, tb.s & 1u);
+    if (tb.t == tb.stop)
+        tb.on = false;
+}
+
+// One step of block r: 8 units x 2 entries x 2 candidates per thread.
+template <bool ARGMIN>
+__device__ __forceinline__ void k1_step(const float *__restrict__ Mloc, const float *Mrem,
+                                        float *__restrict__ Mn, const float y,
+                                        const uint32_t (&vpk)[16], const int r, const int tid,
+                                        uint32_t &word, unsigned long long &key) {
+    word = 0u;
+    float mr[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++)   // the peer's costs first: the longest latency
+        mr[u] = Mrem[r * 8192 + u * 1024 + tid];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const int hp = r * 8192 + u * 1024 + tid;
+        const float ml = Mloc[hp];
+        const float m0 = r == 0 ? ml : mr[u];   // M(h')        (block 0's half)
+        const float m1 = r == 0 ? mr[u] : ml;   // M(16384 + h') (block 1's half)
+        int best0, best1;
+        uint32_t bk0, bk1;
+        acs_pair<true>(m0, vpk[u * 2 + 0], y, 0, best0, best1, bk0, bk1);
+        acs_pair<true>(m1, vpk[u * 2 + 1], y, 1, best0, best1, bk0, bk1);
+        word |= (bk0 << (2 * u)) | (bk1 << (2 * u + 1));
+        if (ARGMIN) {
+            const uint32_t g0 = 2u * (uint32_t)hp;
+            const unsigned long long k0 =
+                ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << 15) | g0);
+            const unsigned long long k1 =
+                ((unsigned long long)(uint32_t)best1 << 32) | ((bk1 << 15) | (g0 + 1u));
+            key = k0 < key ? k0 : key;
+            key = k1 < key ? k1 : key;
+        } else {
+            *reinterpret_cast<float2 *>(Mn + 2 * (u * 1024 + tid)) =
+                make_float2(__int_as_float(best0), __int_as_float(best1));
+        }
+    }
+}
+
+template <int TT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    encode_k1_kernel(const EncodeLaunch a) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int r = (int)cluster.block_rank();
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *M0 = reinterpret_cast<float *>(smem);
+    float *M1 = M0 + kHalfK1;
+    float *ys = M1 + kHalfK1;
+    uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
+    __shared__ uint32_t sh_sstar[2], sh_end[2];
+    __shared__ unsigned long long sh_key;
+    __shared__ Tb tb;
+    const float *R0 = cluster.map_shared_rank(M0, 1 - r);
+    const float *R1 = cluster.map_shared_rank(M1, 1 - r);
+
+    const int tid = threadIdx.x;
+    uint32_t vpk[16];
+#pragma unroll
+    for (int u = 0; u < 8; u++)
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const uint32_t hp = (uint32_t)(r * 8192 + u * 1024 + tid);
+            const uint32_t s0 = ((uint32_t)k << 15) | (2u * hp);
+            vpk[u * 2 + k] = (uint32_t)__half_as_ushort(mul1_half(s0)) |
+                             ((uint32_t)__half_as_ushort(mul1_half(s0 + 1u)) << 16);
+        }
+
+    const float inv_s = a.inv_scale_dev ? __ldg(a.inv_scale_dev) : a.inv_scale;
+    const int T = TT ? TT : a.T;
+    const int half = T / 2;
+    const int code_words = T / 32;
+    const bool row_tiles = TT == 0;
+    const int tiles_c = row_tiles ? 1 : (int)(a.cols / 16);
+    const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
+    const int cid = (int)blockIdx.x >> 1;
+    const int n_clusters = (int)gridDim.x >> 1;
+    const int n_my = n_tiles > cid ? (n_tiles - cid + n_clusters - 1) / n_clusters : 0;
+    uint32_t *const scr = a.scratch + (size_t)blockIdx.x * kBlockWords;       // own slice
+    uint32_t *const scr0 = a.scratch + (size_t)(2 * cid) * kBlockWords;       // block 0's slice
+    constexpr size_t kP1 = (size_t)kRowsPass1 * kRowWords, kP2 = (size_t)kRowsPass2 * kRowWords;
+
+    if (tid == 0) {
+        tb.on = false;
+        tb.rows = nullptr;
+        tb.tile = 0;
+        tb.s = tb.pending = 0u;
+        tb.t = tb.stop = tb.row0 = tb.pass = tb.slot = 0;
+        sh_end[0] = sh_end[1] = sh_sstar[0] = sh_sstar[1] = 0u;
+    }
+    cluster_sync();
+
+    const int npairs = (n_my + 1) / 2;
+    for (int ph = 0; ph <= npairs * 4; ph++) {
+        const int p = ph >> 2;
+        const int sub = ph & 3;
+        int f_slot = 0, f_pass = 0, b_slot = 0, b_pass = 0;
+        int f_loc = -1, b_loc = -1;
+        if (p < npairs) {
+            const int A = 2 * p, B = 2 * p + 1;
+            const bool hasB = B < n_my;
+            if (sub == 0) {
+                f_slot = 0; f_pass = 1; f_loc = A;
+                if (p > 0) { b_slot = 1; b_pass = 2; b_loc = 2 * p - 1; }
+            } else if (sub == 1) {
+                if (hasB) { f_slot = 1; f_pass = 1; f_loc = B; }
+                b_slot = 0; b_pass = 1; b_loc = A;
+            } else if (sub == 2) {
+                f_slot = 0; f_pass = 2; f_loc = A;
+                if (hasB) { b_slot = 1; b_pass = 1; b_loc = B; }
+            } else {
+                if (hasB) { f_slot = 1; f_pass = 2; f_loc = B; }
+                b_slot = 0; b_pass = 2; b_loc = A;
+            }
+        } else if (p > 0 && 2 * p - 1 < n_my) {
+            b_slot = 1; b_pass = 2; b_loc = 2 * p - 1;
+        }
+        const bool fwd = f_loc >= 0;
+        const int f_tile = cid + f_loc * n_clusters;
+
+        // block 1 takes end_state from block 0 (written before the last cluster barrier)
+        if (r == 1 && tid == 0) {
+            const uint32_t *rend = cluster.map_shared_rank(sh_end, 0);
+            sh_end[0] = rend[0];
+            sh_end[1] = rend[1];
+        }
+        __syncthreads();
+
+        if (fwd) {
+            if (tid < T) {
+                const int i = (f_pass == 1) ? (tid + half < T ? tid + half : tid + half - T) : tid;
+                const float *src;
+                if (row_tiles) {
+                    src = a.Y + (size_t)f_tile * (size_t)T + i;
+                } else {
+                    const int tr = f_tile / tiles_c, tc = f_tile % tiles_c;
+                    src = a.Y + (size_t)(tr * 16 + (i >> 4)) * (size_t)a.cols + tc * 16 + (i & 15);
+                }
+                ys[tid] = __fmul_rn(__ldg(src), inv_s);
+            }
+            if (f_pass == 1) {
+                for (int g = tid; g < kHalfK1; g += kThreads)
+                    M0[g] = 0.0f;
+            } else {
+                const int ge = (int)(sh_end[f_slot] & 0x7FFFu) - r * kHalfK1;
+                for (int g = tid; g < kHalfK1; g += kThreads)
+                    M0[g] = (g == ge) ? 0.0f : __int_as_float(0x7f800000);
+            }
+        }
+        if (r == 0 && tid == 0 && b_loc >= 0) {
+            tb.on = true;
+            tb.pass = b_pass;
+            tb.slot = b_slot;
+            tb.tile = cid + b_loc * n_clusters;
+            tb.t = T - 1;
+            if (b_pass == 1) {
+                tb.s = sh_sstar[b_slot];
+                tb.stop = half - 1;
+                tb.rows = scr0 + (size_t)b_slot * kP1;
+                tb.row0 = half - 1;
+            } else {
+                tb.s = sh_end[b_slot];
+                tb.stop = 0;
+                tb.rows = scr0 + 2 * kP1 + (size_t)b_slot * kP2;
+                tb.row0 = 0;
+                for (int w = 0; w < code_words; w++)
+                    bs[w] = 0u;
+                put_code<1>(bs, T - 1, tb.s & 1u);
+            }
+        }
+        cluster_sync();
+
+        if (fwd) {
+            uint32_t *rows = (f_pass == 1) ? scr + (size_t)f_slot * kP1
+                                           : scr + 2 * kP1 + (size_t)f_slot * kP2;
+            const int row0 = (f_pass == 1) ? half - 1 : 0;
+            for (int t = 0; t < T - 1; t++) {
+                if (r == 0 && tid == 0 && tb.on)
+                    k1_tb_issue(tb);
+                const float *Mp = (t & 1) ? M1 : M0;
+                const float *Rp = (t & 1) ? R1 : R0;
+                float *Mn = (t & 1) ? M0 : M1;
+                uint32_t word;
+                unsigned long long key = 0ull;
+                k1_step<false>(Mp, Rp, Mn, ys[t], vpk, r, tid, word, key);
+                if (t >= row0)
+                    rows[(size_t)(t - row0) * kRowWords + tid] = word;
+                if (r == 0 && tid == 0 && tb.on)
+                    k1_tb_advance(tb, bs);
+                cluster_sync();
+            }
+            if (f_pass == 1) {
+                // last step (T even: reads M_{T-2} from M1 / R1)
+                if (r == 0 && tid == 0 && tb.on)
+                    k1_tb_issue(tb);
+                uint32_t word;
+                unsigned long long key = ~0ull;
+                k1_step<true>(M1, R1, nullptr, ys[T - 1], vpk, r, tid, word, key);
+                if (r == 0 && tid == 0 && tb.on)
+                    k1_tb_advance(tb, bs);
+                key = warp_min_u64(key);
+                if ((tid & 31) == 0)
+                    red[tid >> 5] = key;
+                __syncthreads();
+                if (tid < 32) {
+                    key = warp_min_u64(red[tid]);
+                    if (tid == 0)
+                        sh_key = key;
+                }
+                cluster_sync();
+                if (r == 0 && tid == 0) {
+                    const unsigned long long k1 = *cluster.map_shared_rank(&sh_key, 1);
+                    const unsigned long long kk = sh_key < k1 ? sh_key : k1;
+                    sh_sstar[f_slot] = (uint32_t)(kk & 0xffffffffull);
+                }
+            } else if (r == 0 && tid == 0 && a.tile_cost) {
+                // fl(M_{T-2}(end >> 1) + q_{T-1}(end)); M_{T-2} is in M1 of its owner
+                const uint32_t e = sh_end[f_slot];
+                const uint32_t ge = e >> 1;
+                const float *src = (ge >> 14) == 0 ? M1 : R1;
+                const float d = __fsub_rn(ys[T - 1], mul1_value(e));
+                a.tile_cost[f_tile] = __fadd_rn(src[ge & 16383u], __fmul_rn(d, d));
+            }
+        }
+        if (r == 0 && tid == 0 && b_loc >= 0) {
+            while (tb.on) {
+                k1_tb_issue(tb);
+                k1_tb_advance(tb, bs);
+            }
+            if (tb.pass == 1) {
+                sh_end[tb.slot] = tb.s;
+            } else {
+                uint32_t *dst = a.codes + (size_t)tb.tile * code_words;
+                for (int w = 0; w < code_words; w++)
+                    dst[w] = bs[w];
+            }
+        }
+        cluster_sync();
+    }
+}
+
+template <int TT>
+exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    const size_t smem = (size_t)(2 * kHalfK1 + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(encode_k1_kernel<TT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaFuncSetAttribute(encode k1)");
+    // tiles are assigned statically to clusters: launch only as many clusters as
+    // can be resident at once, so none starts its share late
+    EncodeLaunch q = p;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    int n_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&n_clusters, (void *)encode_k1_kernel<TT>, &cfg);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaOccupancyMaxActiveClusters(encode k1)");
+    if (n_clusters < 1)
+        return set_error(EXL3_ERR_CUDA, "no two-block cluster of the K=1 encoder fits this GPU");
+    if (2 * n_clusters < q.grid)
+        q.grid = 2 * n_clusters;
+    if (profiled)
+        profile_encode_begin(s);
+    encode_k1_kernel<TT><<<q.grid, kThreads, smem, s>>>(q);
+    if (profiled) {
+        note_launch();
+        profile_encode_end(s);
+    }
+    return cuda_check(cudaGetLastError(), "encode k1 launch");
+}
+
+}  // namespace
+
+exl3_status launch_encode_k1(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    if (p.grid < 2 || (p.grid & 1))
+        return set_error(EXL3_ERR_WORKSPACE, "K=1 needs an even number (>= 2) of blocks, got %d",
+                         p.grid);
+    if (p.row_tiles)
+        return launch_k1_t<0>(p, s, profiled);
+    return launch_k1_t<256>(p, s, profiled);
+}
+
+}  // namespace exl3

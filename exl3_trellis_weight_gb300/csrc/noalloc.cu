@@ -74,7 +74,7 @@ extern "C" EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_
         return set_error(EXL3_ERR_INVALID_ARG, "matrix %lldx%lld is too large", (long long)rows,
                          (long long)cols);
     if (K < 2 || K > 4)
-        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: this build encodes K in {2,3,4}", K);
+        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: the workspace-free encode takes K in {2,3,4}", K);
     if (!(scale > 0.0f) || !(scale < __builtin_inff()))
         return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
     if (blocks < 0 || blocks > kNoAllocMaxBlocks)

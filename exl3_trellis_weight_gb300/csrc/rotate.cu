@@ -61,6 +61,7 @@ __device__ __forceinline__ uint32_t window_state(const uint32_t *w, int i) {
 
 __device__ __forceinline__ uint32_t window_state_k(const uint32_t *w, int i, int K) {
     switch (K) {
+    case 1: return window_state<1>(w, i);
     case 2: return window_state<2>(w, i);
     case 3: return window_state<3>(w, i);
     default: return window_state<4>(w, i);

@@ -70,7 +70,7 @@ EXL3_API const char *exl3_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 EXL3_API int exl3_version(void);
 
-/* 1 if this build encodes at K bits per weight, else 0.  K in {2, 3, 4}. */
+/* 1 if this build encodes at K bits per weight, else 0.  K in {1, 2, 3, 4}. */
 EXL3_API int exl3_supports_k(int K);
 
 /*
@@ -112,7 +112,10 @@ EXL3_API size_t exl3_encode_workspace_min_bytes(int K);
  *
  *   Y      (device) fp32 [rows, cols], the rotated matrix; targets are
  *          y = fl(Y * fl32(1/scale)).
- *   rows, cols: positive multiples of 16.   K in {2, 3, 4}.   scale > 0, finite.
+ *   rows, cols: positive multiples of 16.   K in {1, 2, 3, 4}.   scale > 0, finite.
+ *   K = 1 runs each tile on a cluster of two blocks (the 2^15-entry cost row is
+ *   split between their shared memories), so its workspace holds an even
+ *   number of block slices (minimum two).
  *   codes  (device, 4-byte aligned) uint16 [rows/16][cols/16][16*K].  For each
  *          tile the codes e_i (low K bits of the chosen state at element i)
  *          form the bitstream e_0 || e_1 || ... || e_255, each code MSB first.
@@ -176,7 +179,7 @@ EXL3_API exl3_status exl3_mse(const void *W, int dt, const float *What, int64_t 
  * 1 when it is 0 (an all-zero matrix); s = fl32(g * sigma); codes = encode(R, s); What = inverse(decode(codes, s));
  * mse = MSE(W, What).
  *   W (device) bf16 or fp32 [rows, cols]; su, sv (device) fp32 sign vectors.
- *   rows, cols multiples of 128; K in {2, 3, 4}; g > 0.
+ *   rows, cols multiples of 128; K in {1, 2, 3, 4}; g > 0.
  *   codes (device) uint16 [rows/16][cols/16][16*K].
  *   scale_out (device) float, the absolute scale s (decode with it).
  *   mse_out (device) double.   sigma_out (device) double or NULL.

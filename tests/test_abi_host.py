@@ -48,7 +48,7 @@ def test_status_strings(ex):
 
 
 def test_supported_k(ex):
-    assert [ex.supports_k(k) for k in range(0, 6)] == [False, False, True, True, True, False]
+    assert [ex.supports_k(k) for k in range(0, 6)] == [False, True, True, True, True, False]
 
 
 FAKE = ctypes.c_void_p(0x10000000)      # 256-byte aligned, never dereferenced
@@ -67,7 +67,8 @@ def test_encode_rejects_bad_arguments(ex):
         return L.exl3_encode_tiles(a["Y"], a["rows"], a["cols"], a["K"], a["scale"], a["codes"],
                                    a["cost"], a["ws"], a["ws_bytes"], a["stream"])
 
-    assert call(K=1) == 2 and call(K=5) == 2               # unsupported K
+    assert call(K=0) == 2 and call(K=5) == 2               # unsupported K
+    assert call(K=1, ws_bytes=ws_min) == 3                 # K=1 needs two block slices
     assert call(rows=40) == 2 and call(cols=24) == 2       # not multiples of 16
     assert call(rows=0) == 1 and call(cols=-16) == 1
     assert call(Y=None) == 1 and call(codes=None) == 1
@@ -116,7 +117,8 @@ def test_workspace_queries_scale_with_work(ex):
     b = ex.encode_workspace_bytes(100000, 2)
     assert 0 < a <= b
     assert a == 10 * ex.encode_workspace_min_bytes(2)
-    assert ex.encode_workspace_bytes(100, 1) == 0
+    assert ex.encode_workspace_bytes(100, 0) == 0
+    assert ex.encode_workspace_min_bytes(1) == 2 * ex.encode_workspace_min_bytes(2)
     assert ex.quantize_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
     assert ex.gss_workspace_bytes(4096, 4096, 2) > ex.quantize_workspace_bytes(4096, 4096, 2)
 

@@ -55,7 +55,7 @@ def rot128():
     return W.numpy()
 
 
-@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
 def test_encode_rot128_bit_exact(ex, rot128, K):
     Y = rot128
     codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=1.0, want_cost=True)
@@ -66,7 +66,7 @@ def test_encode_rot128_bit_exact(ex, rot128, K):
     assert np.array_equal(cost.cpu().numpy().view(np.uint32), wcost.view(np.uint32))
 
 
-@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
 @pytest.mark.parametrize("blocks", [None, 1, 4])
 def test_encode_ragged_tiles_and_small_grids(ex, K, blocks):
     """15 tiles (3x5, not a multiple of the pair pipeline); 1 block walks all
@@ -75,6 +75,7 @@ def test_encode_ragged_tiles_and_small_grids(ex, K, blocks):
     Y = rng.standard_normal((48, 80)).astype(np.float32) * 0.7
     ws = None
     if blocks is not None:
+        # the minimum workspace is one block slice (two, i.e. one cluster, at K=1)
         ws = torch.empty(blocks * ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
     codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=0.7, want_cost=True, ws=ws)
     torch.cuda.synchronize()
@@ -97,7 +98,7 @@ def _edge_inputs():
 
 
 @pytest.mark.parametrize("name,Y", list(_edge_inputs()), ids=[n for n, _ in _edge_inputs()])
-@pytest.mark.parametrize("K", [2, 4])
+@pytest.mark.parametrize("K", [1, 2, 4])
 def test_encode_edge_inputs_bit_exact(ex, name, Y, K):
     codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=1.0, want_cost=True)
     torch.cuda.synchronize()
@@ -121,7 +122,7 @@ def test_encode_single_tile_and_repeatability(ex):
 # decode, rotation, MSE
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
 def test_decode_random_codes_bit_exact(ex, K):
     rows, cols = 512, 1024 if K == 4 else 256
     rng = np.random.default_rng(K)
@@ -187,7 +188,8 @@ def test_mse_fixed_order(ex, dt):
 # full chain and golden-section search
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rows,cols,K,seed", [(256, 256, 2, 21), (128, 256, 3, 22), (256, 128, 4, 23)])
+@pytest.mark.parametrize("rows,cols,K,seed", [(256, 256, 2, 21), (128, 256, 3, 22), (256, 128, 4, 23),
+                                              (128, 128, 1, 24)])
 def test_quantize_chain_matches_oracle(ex, rows, cols, K, seed):
     W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02, outlier_frac=0.001)
     su, sv = inputs.sign_pair(rows, cols, seed)
@@ -290,6 +292,12 @@ def test_full_mlp12288_k4_sampled(ex):
     _check_full(ex, W, su, sv, K, 24, 2)
 
 
+def test_full_linear4096_k1_sampled(ex):
+    """K=1 (two-block clusters) at full size, the bench's launch configuration."""
+    (_, W, su, sv, _), = inputs.workload("linear4096_k2")
+    _check_full(ex, W, su, sv, 1, 24, 5)
+
+
 @pytest.mark.parametrize("proj", ["k", "down"])
 def test_full_layer_k3_sampled(ex, proj):
     for lab, W, su, sv, K in inputs.workload("layer4096_k3"):
@@ -338,7 +346,8 @@ def test_profile_counts_launches(ex):
 # rows of T targets (non-256 tile lengths)
 # ---------------------------------------------------------------------------
 
-ROW_CASES = [(160, 2), (160, 3), (160, 4), (16, 2), (48, 2), (96, 3), (64, 4), (256, 2), (32, 4)]
+ROW_CASES = [(160, 1), (160, 2), (160, 3), (160, 4), (16, 2), (48, 2), (96, 3), (64, 4), (256, 2),
+             (32, 4), (64, 1)]
 
 
 @pytest.mark.parametrize("T,K", ROW_CASES)
