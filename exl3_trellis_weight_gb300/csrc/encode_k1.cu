@@ -3,13 +3,17 @@
 //
 // At K = 1 the tracked cost row has 2^15 fp32 entries (128 KiB); two copies do
 // not fit one SM's shared memory.  A tile is therefore encoded by a cluster of
-// two 1024-thread blocks on two SMs.  Block r of the cluster holds the half of
-// the row whose top index bit is r, double-buffered in its shared memory:
-//   unit h' (tracked entries 2h', 2h'+1) reads M(h') and M(16384 + h'): one cost
-//   in each half (ld.shared::cluster for the peer's, a plain load for its own)
-//   and writes M(2h'), M(2h'+1), which lie in the half of block h' >> 13.
-// Block r handles the 8192 units h' = r*8192 + u*1024 + tid (u = 0..7), so all
-// of its writes are local.  One cluster barrier separates consecutive steps.
+// two 1024-thread blocks on two SMs.  Unit h' (tracked entries 2h', 2h'+1)
+// reads M(h') and M(16384 + h'); block r handles the 8192 units
+// h' = r*8192 + u*1024 + tid (u = 0..7) and keeps, double-buffered in its
+// shared memory, exactly the costs its units read:
+//   A[i] = M(r*8192 + i),  B[i] = M(16384 + r*8192 + i),  i in [0, 8192).
+// The writer pushes: entry g = 2h' + j produced by block r is read next step by
+// block (g >> 13) & 1 (= u >> 2) as its A (r = 0) or B (r = 1) value at index
+// g & 8191, so units u < 4 store into block 0 and u >= 4 into block 1 (plain
+// st.shared::cluster through the mapped address; no multicast).  Every read is
+// local.  One cluster barrier separates consecutive steps; its release orders
+// the pushed stores before the peer's reads.
 //
 // Everything else follows encode.cu: the same two passes, tie rules, packing,
 // 1024-word decision rows (each block writes the rows of its own entries into
@@ -25,12 +29,31 @@ namespace exl3 {
 
 namespace {
 
-constexpr int kHalfK1 = 16384;   // tracked entries per block
 constexpr size_t kBlockWords = kEncodeBlockScratchBytes / sizeof(uint32_t);
 
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair
+// (same operations as cand_pair<true>, without the add)
+__device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const float y) {
+    unsigned long long q;
+    asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
+        "mov.b32 {hl, hh}, %1;\n\t"
+        "sub.rn.f32.f16 a, hl, %2;\n\t"
+        "sub.rn.f32.f16 b, hh, %2;\n\t"
+        "mov.b64 d, {a, b};\n\t"
+        "mul.rn.f32x2 %0, d, d;\n\t}"
+        : "=l"(q) : "r"(vw), "f"(y));
+    return q;
 }
 
 // Where D_t(g) of tracked entry g (15 bits) lives: owner block, word, bit.
@@ -62,30 +85,34 @@ __device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
         tb.on = false;
 }
 
-// One step of block r: 8 units x 2 entries x 2 candidates per thread.
+// One step of block r: 8 units x 2 entries x 2 candidates per thread.  The
+// squares q[u*2 + k] (entries 2h', 2h'+1 of unit u, candidate k) were computed
+// beforehand (they do not depend on the cost row).  A, B: this block's read
+// buffer; dst0 / dst1: the next-step array of block 0 / block 1 this block
+// writes into (its own or the peer's, mapped).
 template <bool ARGMIN>
-__device__ __forceinline__ void k1_step(const float *__restrict__ Mloc, const float *Mrem,
-                                        float *__restrict__ Mn, const float y,
-                                        const uint32_t (&vpk)[16], const int r, const int tid,
-                                        uint32_t &word, unsigned long long &key) {
+__device__ __forceinline__ void k1_step(const float *__restrict__ A, const float *__restrict__ B,
+                                        float *dst0, float *dst1,
+                                        const unsigned long long (&q)[16], const int r,
+                                        const int tid, uint32_t &word, unsigned long long &key) {
     word = 0u;
-    float mr[8];
-#pragma unroll
-    for (int u = 0; u < 8; u++)   // the peer's costs first: the longest latency
-        mr[u] = Mrem[r * 8192 + u * 1024 + tid];
 #pragma unroll
     for (int u = 0; u < 8; u++) {
-        const int hp = r * 8192 + u * 1024 + tid;
-        const float ml = Mloc[hp];
-        const float m0 = r == 0 ? ml : mr[u];   // M(h')        (block 0's half)
-        const float m1 = r == 0 ? mr[u] : ml;   // M(16384 + h') (block 1's half)
-        int best0, best1;
-        uint32_t bk0, bk1;
-        acs_pair<true>(m0, vpk[u * 2 + 0], y, 0, best0, best1, bk0, bk1);
-        acs_pair<true>(m1, vpk[u * 2 + 1], y, 1, best0, best1, bk0, bk1);
+        const int i = u * 1024 + tid;
+        const float m0 = A[i];   // M(h')
+        const float m1 = B[i];   // M(16384 + h')
+        const unsigned long long q0 = q[u * 2 + 0], q1 = q[u * 2 + 1];
+        int best0 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 & 0xffffffffull))));
+        int best1 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 >> 32))));
+        const int c0 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 & 0xffffffffull))));
+        const int c1 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 >> 32))));
+        bool keep0, keep1;
+        best0 = __vibmin_s32(best0, c0, &keep0);   // ties keep k = 0
+        best1 = __vibmin_s32(best1, c1, &keep1);
+        const uint32_t bk0 = keep0 ? 0u : 1u, bk1 = keep1 ? 0u : 1u;
         word |= (bk0 << (2 * u)) | (bk1 << (2 * u + 1));
         if (ARGMIN) {
-            const uint32_t g0 = 2u * (uint32_t)hp;
+            const uint32_t g0 = 2u * (uint32_t)(r * 8192 + i);
             const unsigned long long k0 =
                 ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << 15) | g0);
             const unsigned long long k1 =
@@ -93,10 +120,18 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ Mloc, const fl
             key = k0 < key ? k0 : key;
             key = k1 < key ? k1 : key;
         } else {
-            *reinterpret_cast<float2 *>(Mn + 2 * (u * 1024 + tid)) =
+            float *dst = (u < 4) ? dst0 : dst1;
+            *reinterpret_cast<float2 *>(dst + 2 * ((u & 3) * 1024 + tid)) =
                 make_float2(__int_as_float(best0), __int_as_float(best1));
         }
     }
+}
+
+__device__ __forceinline__ void k1_squares(const uint32_t (&vpk)[16], const float y,
+                                           unsigned long long (&q)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; i++)
+        q[i] = sq_pair(vpk[i], y);
 }
 
 template <int TT>
@@ -105,16 +140,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
     extern __shared__ __align__(16) unsigned char smem[];
-    float *M0 = reinterpret_cast<float *>(smem);
-    float *M1 = M0 + kHalfK1;
-    float *ys = M1 + kHalfK1;
+    // read buffers: buf b holds A_b[8192] then B_b[8192]
+    float *A0 = reinterpret_cast<float *>(smem);
+    float *B0 = A0 + 8192;
+    float *A1 = B0 + 8192;
+    float *B1 = A1 + 8192;
+    float *ys = B1 + 8192;
     uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
     __shared__ uint32_t sh_sstar[2], sh_end[2];
     __shared__ unsigned long long sh_key;
     __shared__ Tb tb;
-    const float *R0 = cluster.map_shared_rank(M0, 1 - r);
-    const float *R1 = cluster.map_shared_rank(M1, 1 - r);
+    // arrays this block writes: its A (r = 0) or B (r = 1) slot, in both blocks
+    float *const own0 = r == 0 ? A0 : B0;
+    float *const own1 = r == 0 ? A1 : B1;
+    float *const W0[2] = {cluster.map_shared_rank(own0, 0), cluster.map_shared_rank(own0, 1)};
+    float *const W1[2] = {cluster.map_shared_rank(own1, 0), cluster.map_shared_rank(own1, 1)};
 
     const int tid = threadIdx.x;
     uint32_t vpk[16];
@@ -201,12 +242,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ys[tid] = __fmul_rn(__ldg(src), inv_s);
             }
             if (f_pass == 1) {
-                for (int g = tid; g < kHalfK1; g += kThreads)
-                    M0[g] = 0.0f;
+                for (int i = tid; i < 8192; i += kThreads) {
+                    A0[i] = 0.0f;
+                    B0[i] = 0.0f;
+                }
             } else {
-                const int ge = (int)(sh_end[f_slot] & 0x7FFFu) - r * kHalfK1;
-                for (int g = tid; g < kHalfK1; g += kThreads)
-                    M0[g] = (g == ge) ? 0.0f : __int_as_float(0x7f800000);
+                const int ge = (int)(sh_end[f_slot] & 0x7FFFu);
+                for (int i = tid; i < 8192; i += kThreads) {
+                    A0[i] = (r * 8192 + i == ge) ? 0.0f : __int_as_float(0x7f800000);
+                    B0[i] = (16384 + r * 8192 + i == ge) ? 0.0f : __int_as_float(0x7f800000);
+                }
             }
         }
         if (r == 0 && tid == 0 && b_loc >= 0) {
@@ -236,28 +281,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t *rows = (f_pass == 1) ? scr + (size_t)f_slot * kP1
                                            : scr + 2 * kP1 + (size_t)f_slot * kP2;
             const int row0 = (f_pass == 1) ? half - 1 : 0;
+            unsigned long long q[16];
+            k1_squares(vpk, ys[0], q);
             for (int t = 0; t < T - 1; t++) {
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_issue(tb);
-                const float *Mp = (t & 1) ? M1 : M0;
-                const float *Rp = (t & 1) ? R1 : R0;
-                float *Mn = (t & 1) ? M0 : M1;
+                const float *Ap = (t & 1) ? A1 : A0;
+                const float *Bp = (t & 1) ? B1 : B0;
+                float *const *Wn = (t & 1) ? W0 : W1;
                 uint32_t word;
                 unsigned long long key = 0ull;
-                k1_step<false>(Mp, Rp, Mn, ys[t], vpk, r, tid, word, key);
+                k1_step<false>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
+                // publish this step's costs, then do the work that needs no peer
+                // data (next squares, decision store, traceback) before waiting
+                cluster_arrive();
+                k1_squares(vpk, ys[t + 1], q);
                 if (t >= row0)
                     rows[(size_t)(t - row0) * kRowWords + tid] = word;
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
-                cluster_sync();
+                cluster_wait();
             }
             if (f_pass == 1) {
-                // last step (T even: reads M_{T-2} from M1 / R1)
+                // last step (T even: reads M_{T-2} from buffer 1); q holds its squares
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_issue(tb);
                 uint32_t word;
                 unsigned long long key = ~0ull;
-                k1_step<true>(M1, R1, nullptr, ys[T - 1], vpk, r, tid, word, key);
+                k1_step<true>(A1, B1, nullptr, nullptr, q, r, tid, word, key);
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
                 key = warp_min_u64(key);
@@ -276,12 +327,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     sh_sstar[f_slot] = (uint32_t)(kk & 0xffffffffull);
                 }
             } else if (r == 0 && tid == 0 && a.tile_cost) {
-                // fl(M_{T-2}(end >> 1) + q_{T-1}(end)); M_{T-2} is in M1 of its owner
+                // fl(M_{T-2}(end >> 1) + q_{T-1}(end)); M_{T-2} is in buffer 1 of the
+                // block that reads it: block (ge >> 13) & 1, array A/B by ge >> 14
                 const uint32_t e = sh_end[f_slot];
                 const uint32_t ge = e >> 1;
-                const float *src = (ge >> 14) == 0 ? M1 : R1;
+                const float *arr = cluster.map_shared_rank((ge >> 14) ? B1 : A1, (int)((ge >> 13) & 1u));
                 const float d = __fsub_rn(ys[T - 1], mul1_value(e));
-                a.tile_cost[f_tile] = __fadd_rn(src[ge & 16383u], __fmul_rn(d, d));
+                a.tile_cost[f_tile] = __fadd_rn(arr[ge & 8191u], __fmul_rn(d, d));
             }
         }
         if (r == 0 && tid == 0 && b_loc >= 0) {
@@ -303,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int TT>
 exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
-    const size_t smem = (size_t)(2 * kHalfK1 + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    const size_t smem = (size_t)(4 * 8192 + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(encode_k1_kernel<TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
