@@ -50,7 +50,7 @@ ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
     # `ncu --set full` on 1,216 tiles (profiles/encode_k2_small.md); the traffic is
     # the decision rows, proportional to the tiles processed.
-    "b2fadfc8ecd3400c86055958aa46dbb2a55aeb8d8e117366d90077e056f95146": 1547184.0,
+    "49cc31fcb344f9cf2c3183bfd2e28d6066f32281c8c1a8e76ca1cd20b5b1605e": 1545517.0,
 }
 
 WORKLOAD = "linear4096_k2"
@@ -371,6 +371,30 @@ def run_ours(args):
               "roofline_frac": ach4 / peak_tops, "achieved_tops": ach4}
         del W4, ws4, codes4
 
+    # ---- auxiliary rows on the same workload: page-1 grid + parabola scale search ----------
+    aux = None
+    if not args.skip_aux:
+        ws_s = torch.empty(ex.scale_search_workspace_bytes(rows, cols, K), dtype=torch.uint8,
+                           device=dev)
+        ex.scale_search(W, su, sv, K, ws=ws_s)
+        torch.cuda.synchronize(dev)
+        ss_ms = []
+        for _ in range(3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rs = ex.scale_search(W, su, sv, K, ws=ws_s)
+            b.record(stream)
+            b.synchronize()
+            ss_ms.append(a.elapsed_time(b))
+        n_max = max(rows, cols) // 16 + 2          # sample slots (diagonal + 2 extremes)
+        aux = {"scale_search": {"ms": sum(ss_ms) / len(ss_ms), "g": float(rs["g"].item()),
+                                "tiles_encoded": 19 * ((n_max + 1) // 2) + 8 * n_max,
+                                "what": "rotate, rms, tile sample, 19 coarse + 7 fine + 1 "
+                                        "parabolic grid points, each a batched encode + "
+                                        "decode + fp64 MSE of the sampled tiles"}}
+        del ws_s
+
     # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -399,6 +423,7 @@ def run_ours(args):
             "roofline": roofline,
             "rotation": rotation,
             "k4": k4,
+            "aux": aux,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -418,6 +443,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-k4", action="store_true")
+    ap.add_argument("--skip-aux", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps

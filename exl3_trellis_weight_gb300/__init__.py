@@ -19,7 +19,7 @@ import threading
 __all__ = [
     "Exl3Error", "lib", "lib_path", "rotate", "encode_tiles", "decode_tiles", "mse",
     "encode_rows", "decode_rows",
-    "quantize", "gss_scale", "encode_workspace_bytes", "encode_workspace_min_bytes",
+    "quantize", "gss_scale", "scale_search", "scale_search_workspace_bytes", "encode_workspace_bytes", "encode_workspace_min_bytes",
     "quantize_workspace_bytes", "gss_workspace_bytes", "mse_workspace_bytes",
     "supports_k", "profile_enable", "profile_read", "EXL3_F32", "EXL3_BF16",
 ]
@@ -80,10 +80,13 @@ def lib():
         L.exl3_gss_workspace_bytes.restype = sz
         L.exl3_gss_scale.argtypes = [P, i32, i64, i64, P, P, i32, f64, f64, i32,
                                      P, P, P, P, P, P, sz, P]
+        L.exl3_scale_search_workspace_bytes.argtypes = [i64, i64, i32]
+        L.exl3_scale_search_workspace_bytes.restype = sz
+        L.exl3_scale_search.argtypes = [P, i32, i64, i64, P, P, i32, P, P, P, P, sz, P]
         L.exl3_profile_enable.argtypes = [i32]
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
-        for name in ("exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
+        for name in ("exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
         _lib = L
@@ -281,6 +284,27 @@ def quantize(W, su, sv, K: int, g: float = 1.0, codes=None, want_What: bool = Fa
                                _ptr(What), _ptr(ws), ws.numel() * ws.element_size(),
                                _stream(dev)))
     return dict(codes=codes, scale=scale, mse=m, sigma=sigma, What=What)
+
+
+def scale_search_workspace_bytes(rows: int, cols: int, K: int) -> int:
+    return int(lib().exl3_scale_search_workspace_bytes(rows, cols, K))
+
+
+def scale_search(W, su, sv, K: int, want_history: bool = True, ws=None):
+    """exl3_scale_search: grid + parabola search for the relative scale on a tile
+    sample.  Returns dict(g, scale, history) as device tensors (history [27, 2])."""
+    torch = _torch()
+    _need_cuda(W, su, sv)
+    rows, cols = W.shape
+    dev = W.device
+    g = torch.empty((), dtype=torch.float64, device=dev)
+    scale = torch.empty((), dtype=torch.float32, device=dev)
+    hist = torch.empty(54, dtype=torch.float64, device=dev) if want_history else None
+    ws = _workspace(scale_search_workspace_bytes(rows, cols, K), dev, ws)
+    _check(lib().exl3_scale_search(_ptr(W), _dt(W), rows, cols, _ptr(su), _ptr(sv), K, _ptr(g),
+                                   _ptr(scale), _ptr(hist), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(dev)))
+    return dict(g=g, scale=scale, history=None if hist is None else hist.view(27, 2))
 
 
 def gss_scale(W, su, sv, K: int, lo: float = 0.5, hi: float = 2.0, n_eval: int = 12,

@@ -674,6 +674,77 @@ exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t cols, co
     return EXL3_OK;
 }
 
+// ---- grid-and-parabola scale search -------------------------------------------
+
+static size_t grid_search_carve(void *ws, int64_t rows, int64_t cols, int K, int grid,
+                                GridSearchLaunch *out) {
+    const int64_t n_tiles = (rows / 16) * (cols / 16);
+    const int max_rows = grid_search_max_rows(rows, cols);
+    Carver c(ws);
+    GridSearchLaunch g{};
+    g.R = (float *)c.take((size_t)rows * cols * sizeof(float));
+    g.tile_sums = (double *)c.take((size_t)n_tiles * sizeof(double));
+    g.tree_scr = (double *)c.take(tree_scratch_doubles(n_tiles) * sizeof(double));
+    g.sum = (double *)c.take(sizeof(double));
+    g.sigma = (double *)c.take(sizeof(double));
+    g.extremes = (int *)c.take(2 * sizeof(int));
+    g.sample = (int *)c.take(grid_search_sample_max(rows, cols) * sizeof(int));
+    g.count = (int *)c.take(sizeof(int));
+    g.state = (double *)c.take(grid_search_state_doubles() * sizeof(double));
+    g.rows_buf = (float *)c.take((size_t)max_rows * 256 * sizeof(float));
+    g.codes_buf = (uint32_t *)c.take((size_t)max_rows * 8 * K * sizeof(uint32_t));
+    g.row_sum = (double *)c.take((size_t)max_rows * sizeof(double));
+    g.s_per_g = (float *)c.take(32 * sizeof(float));
+    g.enc = (uint32_t *)c.take((size_t)grid * kEncodeBlockScratchBytes);
+    g.grid = grid;
+    if (out)
+        *out = g;
+    return c.off;
+}
+
+size_t exl3_scale_search_workspace_bytes(int64_t rows, int64_t cols, int K) {
+    if (!k_ok(K) || rows <= 0 || cols <= 0)
+        return 0;
+    const int max_rows = grid_search_max_rows(rows, cols);
+    return grid_search_carve(nullptr, rows, cols, K, encode_grid_full(max_rows, K), nullptr);
+}
+
+exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int64_t cols, const float *su,
+                              const float *sv, int K, double *g_out, float *scale_out,
+                              double *history_out, void *ws, size_t ws_bytes, void *stream) {
+    exl3_status st;
+    if ((st = quant_common_checks(W, dt, rows, cols, su, sv, K)) != EXL3_OK) return st;
+    if ((st = check_ptr(g_out, "g_out", 8)) != EXL3_OK) return st;
+    if (scale_out && !aligned(scale_out, 4))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale_out is not 4-byte aligned");
+    if (history_out && !aligned(history_out, 8))
+        return set_error(EXL3_ERR_INVALID_ARG, "history_out is not 8-byte aligned");
+    if (grid_search_sample_max(rows, cols) > 2048)
+        return set_error(EXL3_ERR_UNSUPPORTED, "rows/16 and cols/16 must be at most 2046");
+    if (!ws || !aligned(ws, kAlign))
+        return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    const size_t fixed = grid_search_carve(nullptr, rows, cols, K, 0, nullptr);
+    if (ws_bytes < fixed)
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes is below the minimum", ws_bytes);
+    const int grid = (int)fit_blocks(encode_grid_full(grid_search_max_rows(rows, cols), K),
+                                     (int64_t)((ws_bytes - fixed) / kEncodeBlockScratchBytes), K);
+    if (grid < 1)
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes is below the minimum", ws_bytes);
+    GridSearchLaunch g{};
+    grid_search_carve(ws, rows, cols, K, grid, &g);
+    g.W = W;
+    g.dt = dt;
+    g.rows = rows;
+    g.cols = cols;
+    g.su = su;
+    g.sv = sv;
+    g.K = K;
+    g.g_out = g_out;
+    g.scale_out = scale_out;
+    g.history = history_out;
+    return run_grid_search(g, (cudaStream_t)stream);
+}
+
 void exl3_profile_enable(int on) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     g_prof_on.store(on != 0);

@@ -152,6 +152,36 @@ struct RotateLaunch {
 };
 exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s);
 
+// grid-and-parabola scale search (scale_search.cu)
+struct GridSearchLaunch {
+    const void *W;
+    int dt;
+    int64_t rows, cols;
+    const float *su, *sv;
+    int K;
+    float *R;               // [rows, cols]
+    double *tile_sums;      // [n_tiles]
+    double *tree_scr;       // tree_scratch_doubles(n_tiles)
+    double *sum, *sigma;    // scalars
+    int *extremes;          // [2]
+    int *sample;            // [sample_max]
+    int *count;             // [1]
+    double *state;          // [grid_search_state_doubles()]
+    float *rows_buf;        // [max_rows, 256]
+    uint32_t *codes_buf;    // [max_rows, 8K]
+    double *row_sum;        // [max_rows]
+    float *s_per_g;         // [19]
+    uint32_t *enc;          // encode scratch, grid blocks
+    int grid;
+    double *g_out;
+    float *scale_out;       // nullable
+    double *history;        // nullable, [2 * 27]
+};
+size_t grid_search_sample_max(int64_t rows, int64_t cols);
+size_t grid_search_state_doubles();
+int grid_search_max_rows(int64_t rows, int64_t cols);
+exl3_status run_grid_search(const GridSearchLaunch &p, cudaStream_t s);
+
 exl3_status launch_tile_sumsq(const void *x, int x_dt, const float *ref, int64_t rows,
                               int64_t cols, double *tile_sums, cudaStream_t s);
 // tree sum of n doubles; scratch >= tree_scratch_doubles(n) doubles; result -> *out

@@ -218,6 +218,39 @@ EXL3_API exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t
                            void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Grid-and-parabola global-scale search on a tile sample (README item 8:
+ * wrapped-diagonal tile sampling with the highest/lowest-RMS tiles, coarse grid
+ * 0.1..1.9 on a strided subsample, fine grid within 0.075 of the coarse
+ * minimum on the full sample, parabolic refinement with a 0.01 floor).  The
+ * README leaves the details open; this library reads them as follows.
+ *   sample   : tiles (i mod TR, i mod TC) for i < max(TR, TC) (TR x TC 16x16
+ *              tiles of R = rotate(W)), then the highest- and lowest-RMS tiles
+ *              (ties to the lower index) when not already in the sample;
+ *   objective: rotated-domain MSE of a subset at s = fl32(g * sigma_R): codes
+ *              from y = fl(r * fl32(1/s)); sum (r - fl(v * s))^2 in fp64,
+ *              row-major per tile, tiles added as a pairwise tree in sample
+ *              order, divided by 256 * tiles;
+ *   coarse   : g = k/10, k = 1..19, on sample entries 0, 2, 4, ...;
+ *   fine     : g_c + 0.025 k, k = -3..3 (g_c the coarse minimum), full sample;
+ *   refine   : when the fine minimum is interior, the vertex of the parabola
+ *              through it and its two neighbours, floored at 0.01, evaluated on
+ *              the full sample and kept if strictly better.
+ * Ties between grid points go to the smaller g.  Everything runs on the device.
+ *   W bf16/fp32 [rows, cols], rows and cols multiples of 128 and at most 32736;
+ *   su, sv fp32 signs; K in {1, 2, 3, 4}.
+ *   g_out (device) double: the chosen relative scale; scale_out (device) float
+ *   or NULL: fl32(g * sigma_R); history_out (device) double [54] or NULL:
+ *   (g, mse) for the 19 coarse points, the 7 fine points and the refinement
+ *   (-1, -1 when it was not valid).
+ *   ws: exl3_scale_search_workspace_bytes(rows, cols, K).
+ */
+EXL3_API size_t exl3_scale_search_workspace_bytes(int64_t rows, int64_t cols, int K);
+EXL3_API exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int64_t cols,
+                                       const float *su, const float *sv, int K, double *g_out,
+                                       float *scale_out, double *history_out, void *ws,
+                                       size_t ws_bytes, void *stream);
+
+/*
  * exl3_encode_tiles without a workspace, for callers that cannot allocate
  * device memory (no counterpart on the pages: an interface addition of this
  * library).  Such callers include plug-ins running inside an application that

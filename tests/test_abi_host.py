@@ -29,7 +29,7 @@ def _declared():
 def test_header_declares_the_path(ex):
     names = _declared()
     for n in ["exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_gss_scale",
-              "exl3_quantize", "exl3_mse"]:
+              "exl3_quantize", "exl3_mse", "exl3_scale_search"]:
         assert n in names
 
 
@@ -110,6 +110,14 @@ def test_rotate_and_quantize_reject_bad_arguments(ex):
     assert gs(2.0, 0.5, 12) == 1
     assert gs(0.0, 2.0, 12) == 1
     assert gs(0.5, 2.0, 12, w=100) == 3
+    sws = ex.scale_search_workspace_bytes(256, 256, 2)
+    sc = lambda rows, cols, K, w=sws, g=FAKE: L.exl3_scale_search(FAKE, 1, rows, cols, FAKE, FAKE, K,
+                                                                  g, None, None, FAKE, w, None)
+    assert sc(256, 200, 2) == 2          # cols not a multiple of 128
+    assert sc(256, 256, 5) == 2
+    assert sc(256, 256, 2, g=None) == 1
+    assert sc(256, 256, 2, w=100) == 3
+    assert sc(32768, 128, 2) == 2        # beyond the 32736-row limit
 
 
 def test_workspace_queries_scale_with_work(ex):
@@ -121,6 +129,8 @@ def test_workspace_queries_scale_with_work(ex):
     assert ex.encode_workspace_min_bytes(1) == 2 * ex.encode_workspace_min_bytes(2)
     assert ex.quantize_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
     assert ex.gss_workspace_bytes(4096, 4096, 2) > ex.quantize_workspace_bytes(4096, 4096, 2)
+    assert ex.scale_search_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
+    assert ex.scale_search_workspace_bytes(4096, 4096, 0) == 0
 
 
 def test_rows_reject_bad_lengths(ex):

@@ -385,3 +385,45 @@ def test_encode_rows_one_block_many_rows(ex):
     for r in range(n_rows):
         st, _, _ = oracle.encode_tile(Y[r], K)
         assert np.array_equal(got[r], oracle.pack(st, K))
+
+
+# ---------------------------------------------------------------------------
+# grid-and-parabola scale search
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols,K,seed", [(128, 256, 2, 61), (256, 128, 3, 62), (128, 128, 4, 63)])
+def test_scale_search_matches_oracle(ex, rows, cols, K, seed):
+    from oracle import scale_search as ss
+    W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02, outlier_frac=0.002)
+    su, sv = inputs.sign_pair(rows, cols, seed)
+    res = ex.scale_search(W.to(DEV), su.to(DEV), sv.to(DEV), K)
+    torch.cuda.synchronize()
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    ref = ss.grid_scale_search(R, K)
+    h = res["history"].cpu().numpy()
+    want = np.array(ref["coarse"] + ref["fine"] +
+                    [ref["refined"] if ref["refined"] is not None else (-1.0, -1.0)])
+    assert np.array_equal(h, want)
+    assert float(res["g"].item()) == ref["g"]
+    assert float(res["scale"].item()) == oracle.scale_for(ref["g"], ref["sigma"])[0]
+
+
+def test_scale_search_full_size_properties(ex):
+    from oracle import scale_search as ss
+    (_, W, su, sv, K), = inputs.workload("linear4096_k2")
+    res = ex.scale_search(W.to(DEV), su.to(DEV), sv.to(DEV), K)
+    torch.cuda.synchronize()
+    h = res["history"].cpu().numpy()
+    g = float(res["g"].item())
+    fine = h[19:26]
+    assert 0.01 <= g <= 1.975
+    # the chosen g is a fine point or the accepted refinement
+    if h[26, 0] >= 0 and h[26, 1] < fine[:, 1].min():
+        assert g == h[26, 0]
+    else:
+        assert g == fine[np.argmin(fine[:, 1]), 0]
+    # recompute the full-sample MSE at the chosen g with the oracle
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    S = ss.sample_tiles(oracle.tile_sumsq(R), 256, 256)
+    f = ss.subset_mse(R, S, K, g, oracle.rms(R))
+    assert f == min(fine[:, 1].min(), h[26, 1] if h[26, 0] >= 0 else np.inf)
