@@ -395,6 +395,49 @@ def run_ours(args):
                                         "decode + fp64 MSE of the sampled tiles"}}
         del ws_s
 
+        # block LDL of a 4096-channel synthetic Hessian and LDLQ of the rotated matrix
+        Hd = inputs.spd_hessian(rows, 50, rho=0.95).to(dev)
+        M = torch.empty(rows, rows, dtype=torch.float32, device=dev)
+        ws_l = torch.empty(ex.block_ldl_workspace_bytes(rows), dtype=torch.uint8, device=dev)
+        ex.block_ldl(Hd, M=M, ws=ws_l)
+        ldl_ms = []
+        for _ in range(2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            _, retries = ex.block_ldl(Hd, M=M, ws=ws_l)
+            b.record(stream)
+            b.synchronize()
+            ldl_ms.append(a.elapsed_time(b))
+        del ws_l
+        R = torch.empty(rows, cols, dtype=torch.float32, device=dev)
+        ex.rotate(W, su, sv, out=R)
+        s_l = float(ex.quantize(W, su, sv, K, 1.0, codes=codes, ws=ws)["scale"].item())
+        ws_q = torch.empty(ex.ldlq_workspace_bytes(rows, cols, K), dtype=torch.uint8, device=dev)
+        codes_q = torch.empty(rows // 16, cols // 16, 16 * K, dtype=torch.int16, device=dev)
+        ex.ldlq(R, M, K, s_l, want_q=False, codes=codes_q, ws=ws_q)
+        torch.cuda.synchronize(dev)
+        ex.profile_enable(True)
+        lq_ms = []
+        for _ in range(2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.ldlq(R, M, K, s_l, want_q=False, codes=codes_q, ws=ws_q)
+            b.record(stream)
+            b.synchronize()
+            lq_ms.append(a.elapsed_time(b))
+        lq_enc_ms, lq_enc_n, _ = ex.profile_read()
+        ex.profile_enable(False)
+        lq_avg = sum(lq_ms) / len(lq_ms)
+        aux["block_ldl"] = {"n": rows, "ms": sum(ldl_ms) / len(ldl_ms), "retries": retries,
+                            "hessian": "spd_hessian(4096, seed 50, rho 0.95): AR(1) channels, "
+                                       "lognormal channel scales, 8192 rows, 1% damping"}
+        aux["ldlq"] = {"ms": lq_avg, "tiles_per_s": n_tiles / (lq_avg / 1e3),
+                       "spans": rows // 16, "tiles_per_span": cols // 16,
+                       "encode_share": (lq_enc_ms / len(lq_ms)) / lq_avg,
+                       "encode_launches": lq_enc_n // len(lq_ms)}
+        del ws_q, codes_q, R, M, Hd
+
     # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:

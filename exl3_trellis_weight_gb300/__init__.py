@@ -83,10 +83,16 @@ def lib():
         L.exl3_scale_search_workspace_bytes.argtypes = [i64, i64, i32]
         L.exl3_scale_search_workspace_bytes.restype = sz
         L.exl3_scale_search.argtypes = [P, i32, i64, i64, P, P, i32, P, P, P, P, sz, P]
+        L.exl3_block_ldl_workspace_bytes.argtypes = [i64]
+        L.exl3_block_ldl_workspace_bytes.restype = sz
+        L.exl3_block_ldl.argtypes = [P, i64, f64, i32, P, P, P, sz, P]
+        L.exl3_ldlq_workspace_bytes.argtypes = [i64, i64, i32]
+        L.exl3_ldlq_workspace_bytes.restype = sz
+        L.exl3_ldlq.argtypes = [P, i64, i64, P, i32, f32, P, P, P, sz, P]
         L.exl3_profile_enable.argtypes = [i32]
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
-        for name in ("exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
+        for name in ("exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
         _lib = L
@@ -305,6 +311,50 @@ def scale_search(W, su, sv, K: int, want_history: bool = True, ws=None):
                                    _ptr(scale), _ptr(hist), _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(dev)))
     return dict(g=g, scale=scale, history=None if hist is None else hist.view(27, 2))
+
+
+def block_ldl_workspace_bytes(n: int) -> int:
+    return int(lib().exl3_block_ldl_workspace_bytes(n))
+
+
+def block_ldl(H, sigma_reg: float = 0.01, max_retries: int = 10, M=None, ws=None):
+    """exl3_block_ldl: M = L blockdiag(L_bb)^-1 (strictly lower block part, fp32)
+    of the damped Cholesky factor of H (fp64 [n, n]).  Returns (M, retries);
+    raises Exl3Error (EXL3_ERR_NUMERIC) when every damping attempt fails."""
+    torch = _torch()
+    _need_cuda(H, M)
+    if H.dtype != torch.float64:
+        raise ValueError("H must be float64")
+    n = H.shape[0]
+    if M is None:
+        M = torch.empty(n, n, dtype=torch.float32, device=H.device)
+    ws = _workspace(block_ldl_workspace_bytes(n), H.device, ws)
+    retries = ctypes.c_int(-1)
+    _check(lib().exl3_block_ldl(_ptr(H), n, ctypes.c_double(sigma_reg), int(max_retries), _ptr(M),
+                                ctypes.byref(retries), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream(H.device)))
+    return M, retries.value
+
+
+def ldlq_workspace_bytes(rows: int, cols: int, K: int) -> int:
+    return int(lib().exl3_ldlq_workspace_bytes(rows, cols, K))
+
+
+def ldlq(R, M, K: int, scale: float, want_q: bool = True, codes=None, ws=None):
+    """exl3_ldlq: span-by-span trellis coding of R (fp32 [rows, cols], input
+    channels down the rows) with error feedback through M.  Returns
+    dict(codes [rows/16, cols/16, 16K] int16, Q fp32 [rows, cols] | None)."""
+    torch = _torch()
+    _need_cuda(R, M, codes)
+    rows, cols = R.shape
+    dev = R.device
+    if codes is None:
+        codes = torch.empty(rows // 16, cols // 16, 16 * K, dtype=torch.int16, device=dev)
+    Q = torch.empty(rows, cols, dtype=torch.float32, device=dev) if want_q else None
+    ws = _workspace(ldlq_workspace_bytes(rows, cols, K), dev, ws)
+    _check(lib().exl3_ldlq(_ptr(R), rows, cols, _ptr(M), K, ctypes.c_float(scale), _ptr(codes),
+                           _ptr(Q), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
+    return dict(codes=codes, Q=Q)
 
 
 def gss_scale(W, su, sv, K: int, lo: float = 0.5, hi: float = 2.0, n_eval: int = 12,

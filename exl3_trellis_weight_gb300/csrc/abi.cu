@@ -389,6 +389,7 @@ const char *exl3_status_str(int status) {
     case EXL3_ERR_UNSUPPORTED: return "EXL3_ERR_UNSUPPORTED";
     case EXL3_ERR_WORKSPACE: return "EXL3_ERR_WORKSPACE";
     case EXL3_ERR_CUDA: return "EXL3_ERR_CUDA";
+    case EXL3_ERR_NUMERIC: return "EXL3_ERR_NUMERIC";
     default: return "EXL3_ERR_UNKNOWN";
     }
 }
@@ -743,6 +744,108 @@ exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int64_t cols,
     g.scale_out = scale_out;
     g.history = history_out;
     return run_grid_search(g, (cudaStream_t)stream);
+}
+
+// ---- block LDL and LDLQ -------------------------------------------------------
+
+static size_t block_ldl_carve(void *ws, int64_t n, BlockLdlLaunch *out) {
+    Carver c(ws);
+    BlockLdlLaunch b{};
+    b.A = (double *)c.take((size_t)n * n * sizeof(double));
+    b.LD = (double *)c.take((size_t)(n / 16) * 256 * sizeof(double));
+    b.delta = (double *)c.take(sizeof(double));
+    b.flag = (int *)c.take(sizeof(int));
+    if (out)
+        *out = b;
+    return c.off;
+}
+
+static bool ldl_dim_ok(int64_t n) { return n >= 16 && n % 16 == 0 && n <= 32768; }
+
+size_t exl3_block_ldl_workspace_bytes(int64_t n) {
+    if (!ldl_dim_ok(n))
+        return 0;
+    return block_ldl_carve(nullptr, n, nullptr);
+}
+
+exl3_status exl3_block_ldl(const double *H, int64_t n, double sigma_reg, int max_retries, float *M,
+                           int *retries_out, void *ws, size_t ws_bytes, void *stream) {
+    exl3_status st;
+    if ((st = check_ptr(H, "H", 8)) != EXL3_OK) return st;
+    if (!ldl_dim_ok(n))
+        return set_error(EXL3_ERR_UNSUPPORTED, "n=%lld: must be a multiple of 16 in [16, 32768]",
+                         (long long)n);
+    if (!(sigma_reg >= 0.0) || !std::isfinite(sigma_reg))
+        return set_error(EXL3_ERR_INVALID_ARG, "sigma_reg must be finite and >= 0");
+    if (max_retries < 0 || max_retries > 100)
+        return set_error(EXL3_ERR_INVALID_ARG, "max_retries=%d outside [0, 100]", max_retries);
+    if ((st = check_ptr(M, "M", 16)) != EXL3_OK) return st;
+    if (!ws || !aligned(ws, kAlign))
+        return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    const size_t need = block_ldl_carve(nullptr, n, nullptr);
+    if (ws_bytes < need)
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, need);
+    BlockLdlLaunch b{};
+    block_ldl_carve(ws, n, &b);
+    b.H = H;
+    b.n = n;
+    b.sigma_reg = sigma_reg;
+    b.max_retries = max_retries;
+    b.M = M;
+    b.retries_out = retries_out;
+    return run_block_ldl(b, (cudaStream_t)stream);
+}
+
+static size_t ldlq_carve(void *ws, int64_t rows, int64_t cols, int grid, LdlqLaunch *out) {
+    Carver c(ws);
+    LdlqLaunch l{};
+    l.acc = (float *)c.take((size_t)rows * cols * sizeof(float));
+    l.U = (float *)c.take((size_t)16 * cols * sizeof(float));
+    l.E = (float *)c.take((size_t)16 * cols * sizeof(float));
+    l.enc = (uint32_t *)c.take((size_t)grid * kEncodeBlockScratchBytes);
+    l.grid = grid;
+    if (out)
+        *out = l;
+    return c.off;
+}
+
+size_t exl3_ldlq_workspace_bytes(int64_t rows, int64_t cols, int K) {
+    if (!k_ok(K) || rows < 16 || cols < 16 || rows % 16 || cols % 16)
+        return 0;
+    return ldlq_carve(nullptr, rows, cols, encode_grid_full(cols / 16, K), nullptr);
+}
+
+exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M, int K, float scale,
+                      uint16_t *codes, float *Q, void *ws, size_t ws_bytes, void *stream) {
+    exl3_status st;
+    if ((st = check_ptr(R, "R", 4)) != EXL3_OK) return st;
+    if (rows < 16 || cols < 16 || rows % 16 || cols % 16)
+        return set_error(EXL3_ERR_UNSUPPORTED, "rows and cols must be positive multiples of 16");
+    if ((st = check_ptr(M, "M", 4)) != EXL3_OK) return st;
+    if ((st = check_k(K)) != EXL3_OK) return st;
+    if (!(scale > 0.0f) || !std::isfinite(scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
+    if (Q && !aligned(Q, 4))
+        return set_error(EXL3_ERR_INVALID_ARG, "Q is not 4-byte aligned");
+    if (!ws || !aligned(ws, kAlign))
+        return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    const size_t fixed = ldlq_carve(nullptr, rows, cols, 0, nullptr);
+    const int64_t cap = ws_bytes > fixed ? (int64_t)((ws_bytes - fixed) / kEncodeBlockScratchBytes) : 0;
+    const int grid = (int)fit_blocks(encode_grid_full(cols / 16, K), cap, K);
+    if (grid < (K == 1 ? 2 : 1))
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes is below the minimum", ws_bytes);
+    LdlqLaunch l{};
+    ldlq_carve(ws, rows, cols, grid, &l);
+    l.R = R;
+    l.rows = rows;
+    l.cols = cols;
+    l.M = M;
+    l.K = K;
+    l.scale = scale;
+    l.codes = reinterpret_cast<uint32_t *>(codes);
+    l.Q = Q;
+    return run_ldlq(l, (cudaStream_t)stream);
 }
 
 void exl3_profile_enable(int on) {

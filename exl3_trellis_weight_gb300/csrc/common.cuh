@@ -40,6 +40,30 @@ __device__ __forceinline__ float mul1_value(uint32_t state) {
     return __half2float(mul1_half(state));
 }
 
+// 16-bit window of a tile's circular code stream ending with the last bit of
+// code i (stream bits [(i+1)K - 16, (i+1)K) modulo 256K, MSB first).
+template <int K>
+__device__ __forceinline__ uint32_t window_state(const uint32_t *w, int i) {
+    constexpr int NB = 256 * K;
+    constexpr int NW = 8 * K;
+    int p = (i + 1) * K - 16;
+    if (p < 0)
+        p += NB;
+    const int wi = p >> 5;
+    const int wj = (wi + 1 == NW) ? 0 : wi + 1;
+    const unsigned long long cat = ((unsigned long long)w[wi] << 32) | w[wj];
+    return (uint32_t)(cat >> (48 - (p & 31))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t window_state_k(const uint32_t *w, int i, int K) {
+    switch (K) {
+    case 1: return window_state<1>(w, i);
+    case 2: return window_state<2>(w, i);
+    case 3: return window_state<3>(w, i);
+    default: return window_state<4>(w, i);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Trellis geometry for K bits per step on the 16-bit bitshift trellis.
 //   tracked row:   G = 2^(16-K) entries, index g = low 16-K bits of a state
@@ -181,6 +205,36 @@ size_t grid_search_sample_max(int64_t rows, int64_t cols);
 size_t grid_search_state_doubles();
 int grid_search_max_rows(int64_t rows, int64_t cols);
 exl3_status run_grid_search(const GridSearchLaunch &p, cudaStream_t s);
+
+// block LDL and LDLQ (ldlq.cu)
+struct BlockLdlLaunch {
+    const double *H;        // [n, n], lower triangle read
+    int64_t n;
+    double sigma_reg;
+    int max_retries;
+    float *M;               // [n, n] out
+    int *retries_out;       // host, nullable
+    double *A;              // [n, n] work (lower triangle)
+    double *LD;             // [n / 16, 16, 16] diagonal blocks of L
+    double *delta;          // scalar
+    int *flag;              // device pivot-failure flag
+};
+exl3_status run_block_ldl(const BlockLdlLaunch &p, cudaStream_t s);
+
+struct LdlqLaunch {
+    const float *R;         // [rows, cols]
+    int64_t rows, cols;
+    const float *M;         // [rows, rows]
+    int K;
+    float scale;
+    uint32_t *codes;        // [rows/16, cols/16, 8K words]
+    float *Q;               // nullable [rows, cols]
+    float *acc;             // [rows, cols]
+    float *U, *E;           // [16, cols] each
+    uint32_t *enc;          // encode scratch, grid blocks
+    int grid;
+};
+exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s);
 
 exl3_status launch_tile_sumsq(const void *x, int x_dt, const float *ref, int64_t rows,
                               int64_t cols, double *tile_sums, cudaStream_t s);

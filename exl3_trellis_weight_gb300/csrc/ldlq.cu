@@ -1,0 +1,381 @@
+// ldlq.cu -- block LDL factorisation of a Hessian and LDLQ error feedback
+// around the trellis tile encoder (page "EXL3 Intel Arc Quantizer", Core
+// Implemented Architecture item 3: blockwise Cholesky/LDL with the inverse of
+// the 16x16 block diagonal folded in, diagonal damping of
+// 2 sigma_reg mean(diag H) retried up to 10 times, and bottom-up error
+// feedback from the strictly lower factor into the targets of the 16-row
+// spans not yet quantised).
+//
+// Arithmetic (the same sequence of IEEE operations as the textbook
+// definitions):
+//   Cholesky, binary64: L[i][j] = (H[i][j] - sum_{k<j} L[i][k] L[j][k]) / L[j][j]
+//     and L[j][j] = sqrt(H[j][j] - sum_{k<j} L[j][k]^2), each term one
+//     rounded product then one rounded difference, k ascending.  The blocked
+//     right-looking schedule below (panels of 16 columns) applies exactly that
+//     sequence to every entry: panel p's 16 terms in ascending k after panel
+//     p-1's, then the entry's own panel.
+//   Fold: X = inverse of each 16x16 diagonal block by forward substitution,
+//     M[i][16b+c] = fl32(sum_{k=c..15} L[i][16b+k] X[k][c]), k ascending.
+//   Feedback, binary32: after span j is coded, every row r above it gets
+//     acc[r][c] = fmaf(M[i][r], E[i][c], acc[r][c]) for i = 16j+15 down to 16j,
+//     E = fl32(R - Q); span b is coded from U = fl32(R + acc).
+#include "common.cuh"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kUpdTile = 64;     // trailing-update tile (64 x 64 entries, 4 x 4 per thread)
+constexpr int kFbRows = 32;      // rows per feedback block
+
+// delta = (2 sigma_reg) * (sum of the diagonal, ascending / n)
+__global__ void __launch_bounds__(1024) diag_delta_kernel(const double *__restrict__ H, int64_t n,
+                                                          double sigma_reg, double *delta) {
+    __shared__ double d[1024];
+    double sum = 0.0;
+    for (int64_t base = 0; base < n; base += 1024) {
+        const int64_t j = base + threadIdx.x;
+        d[threadIdx.x] = j < n ? H[j * n + j] : 0.0;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int m = (int)((n - base) < 1024 ? (n - base) : 1024);
+            for (int t = 0; t < m; t++)
+                sum = __dadd_rn(sum, d[t]);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        *delta = __dmul_rn(__dmul_rn(2.0, sigma_reg), __ddiv_rn(sum, (double)n));
+}
+
+// A = lower triangle of H with a * delta added to the diagonal; clears the flag
+__global__ void chol_init_kernel(const double *__restrict__ H, double *__restrict__ A, int64_t n,
+                                 int a, const double *delta, int *flag) {
+    const int64_t i = blockIdx.y;
+    if (i == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        *flag = 0;
+    const double add = __dmul_rn((double)a, *delta);
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= i;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        double v = H[i * n + j];
+        if (j == i)
+            v = __dadd_rn(v, add);
+        A[i * n + j] = v;
+    }
+}
+
+// Panel p0 (columns p0 .. p0+15).  Every block factors the 16x16 diagonal
+// block in shared memory (identically); block 0 stores it to LD (the rows of A
+// inside the diagonal block are left as they are, so no block reads a value
+// another one has overwritten).  Then one row i >= p0 + 16 per thread:
+// L[i][p0+j] = (A[i][p0+j] - sum_{k<j} L[i][p0+k] L[p0+j][p0+k]) / L[p0+j][p0+j].
+__global__ void __launch_bounds__(256) chol_panel_kernel(double *__restrict__ A, double *__restrict__ LD,
+                                                         int64_t n, int64_t p0, int *flag) {
+    __shared__ double D[16][17];
+    const int t = threadIdx.x;
+    {
+        const int r = t >> 4, c = t & 15;
+        D[r][c] = (c <= r) ? A[(p0 + r) * n + p0 + c] : 0.0;
+    }
+    __syncthreads();
+    if (t < 32) {
+        const int r = t & 15;     // lanes 16..31 repeat lanes 0..15 and never store
+        for (int j = 0; j < 16; j++) {
+            double acc = D[r][j];
+            for (int k = 0; k < j; k++)
+                acc = __dsub_rn(acc, __dmul_rn(D[r][k], D[j][k]));
+            __syncwarp();
+            if (t == j) {
+                double d = 1.0;
+                if (acc > 0.0)
+                    d = __dsqrt_rn(acc);
+                else
+                    *flag = 1;           // not positive definite: the attempt fails
+                D[j][j] = d;
+            }
+            __syncwarp();
+            if (t < 16 && r > j)
+                D[r][j] = __ddiv_rn(acc, D[j][j]);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        const int r = t >> 4, c = t & 15;
+        LD[r * 16 + c] = D[r][c];
+    }
+    const int64_t i = p0 + 16 + (int64_t)blockIdx.x * blockDim.x + t;
+    if (i >= n)
+        return;
+    double *row = A + i * n + p0;
+    double l[16];
+#pragma unroll
+    for (int c = 0; c < 16; c++)
+        l[c] = row[c];
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        double acc = l[j];
+#pragma unroll
+        for (int k = 0; k < j; k++)
+            acc = __dsub_rn(acc, __dmul_rn(l[k], D[j][k]));
+        l[j] = __ddiv_rn(acc, D[j][j]);
+    }
+#pragma unroll
+    for (int c = 0; c < 16; c++)
+        row[c] = l[c];
+}
+
+// Trailing update after panel p0: A[i][j] -= L[i][p0+k] L[j][p0+k], k = 0..15
+// ascending, for p0 + 16 <= j <= i < n.  64 x 64 tiles on or below the
+// diagonal; thread (ty, tx) owns entries (ty + 16a, tx + 16b).
+__global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ A, int64_t n,
+                                                          int64_t p0) {
+    const int ti = blockIdx.y, tj = blockIdx.x;
+    if (tj > ti)
+        return;
+    __shared__ double Li[kUpdTile][17], Lj[kUpdTile][17];
+    const int t = threadIdx.x;
+    const int64_t p1 = p0 + 16;
+    const int64_t i0 = p1 + (int64_t)kUpdTile * ti, j0 = p1 + (int64_t)kUpdTile * tj;
+    for (int e = t; e < kUpdTile * 16; e += 256) {
+        const int r = e >> 4, k = e & 15;
+        Li[r][k] = (i0 + r < n) ? A[(i0 + r) * n + p0 + k] : 0.0;
+        Lj[r][k] = (j0 + r < n) ? A[(j0 + r) * n + p0 + k] : 0.0;
+    }
+    __syncthreads();
+    const int tx = t & 15, ty = t >> 4;
+    double acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const int64_t gi = i0 + ty + 16 * a, gj = j0 + tx + 16 * b;
+            acc[a][b] = (gi < n && gj <= gi) ? A[gi * n + gj] : 0.0;
+        }
+#pragma unroll
+    for (int k = 0; k < 16; k++) {
+        double lj[4];
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+            lj[b] = Lj[tx + 16 * b][k];
+#pragma unroll
+        for (int a = 0; a < 4; a++) {
+            const double li = Li[ty + 16 * a][k];
+#pragma unroll
+            for (int b = 0; b < 4; b++)
+                acc[a][b] = __dsub_rn(acc[a][b], __dmul_rn(li, lj[b]));
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const int64_t gi = i0 + ty + 16 * a, gj = j0 + tx + 16 * b;
+            if (gi < n && gj <= gi)
+                A[gi * n + gj] = acc[a][b];
+        }
+}
+
+// M[i][16b + c] = fl32(sum_{k=c..15} L[i][16b+k] X[k][c]) for rows i >= 16(b+1),
+// X the inverse of diagonal block b (forward substitution by 16 lanes, one
+// column each: X[c][c] = 1 / B[c][c]; X[r][c] = -(sum_{k=c..r-1} B[r][k] X[k][c]) / B[r][r]).
+__global__ void __launch_bounds__(256) ldl_fold_kernel(const double *__restrict__ A,
+                                                       const double *__restrict__ LD, int64_t n,
+                                                       float *__restrict__ M) {
+    const int64_t b = blockIdx.y;
+    __shared__ double X[16][17];
+    const int t = threadIdx.x;
+    const double *B = LD + b * 256;
+    if (t < 16) {
+        const int c = t;
+        for (int r = 0; r < 16; r++)
+            X[r][c] = 0.0;
+        X[c][c] = __ddiv_rn(1.0, B[c * 16 + c]);
+        for (int r = c + 1; r < 16; r++) {
+            double acc = 0.0;
+            for (int k = c; k < r; k++)
+                acc = __dadd_rn(acc, __dmul_rn(B[r * 16 + k], X[k][c]));
+            X[r][c] = __ddiv_rn(-acc, B[r * 16 + r]);
+        }
+    }
+    __syncthreads();
+    const int64_t i = 16 * (b + 1) + (int64_t)blockIdx.x * blockDim.x + t;
+    if (i >= n)
+        return;
+    double l[16];
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+        l[k] = A[i * n + 16 * b + k];
+    float out[16];
+#pragma unroll
+    for (int c = 0; c < 16; c++) {
+        double acc = 0.0;
+#pragma unroll
+        for (int k = c; k < 16; k++)
+            acc = __dadd_rn(acc, __dmul_rn(l[k], X[k][c]));
+        out[c] = __double2float_rn(acc);
+    }
+    float4 *dst = reinterpret_cast<float4 *>(M + i * n + 16 * b);
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+        dst[q] = make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+}
+
+// targets of the first (bottom) span: U = fl32(R + 0)
+__global__ void ldlq_first_target_kernel(const float *__restrict__ R, int64_t cols, int64_t row0,
+                                         float *__restrict__ U) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < 16 * cols)
+        U[e] = __fadd_rn(R[row0 * cols + e], 0.0f);
+}
+
+// one block (256 threads) per tile of the span at rows row0 .. row0+15:
+// q = fl32(v(state) * s), E = fl32(R - q); Q optional
+__global__ void __launch_bounds__(256) ldlq_error_kernel(const uint32_t *__restrict__ codes, int K,
+                                                         const float *__restrict__ R, int64_t cols,
+                                                         int64_t row0, float s, float *__restrict__ E,
+                                                         float *__restrict__ Q) {
+    __shared__ uint32_t cw[32];
+    const int64_t tile = blockIdx.x;
+    const int NW = 8 * K;
+    if (threadIdx.x < NW)
+        cw[threadIdx.x] = codes[tile * NW + threadIdx.x];
+    __syncthreads();
+    const int i = threadIdx.x;
+    const int64_t r = i >> 4, c = tile * 16 + (i & 15);
+    const float q = __fmul_rn(mul1_value(window_state_k(cw, i, K)), s);
+    E[r * cols + c] = __fsub_rn(R[(row0 + r) * cols + c], q);
+    if (Q)
+        Q[(row0 + r) * cols + c] = q;
+}
+
+// after span j: rows r < 16 j, acc = fmaf(M[i][r], E[i - 16j][c], acc) for
+// i = 16j+15 down to 16j; the rows of span j-1 get their targets
+// U = fl32(R + acc) (their accumulator is not needed any more)
+__global__ void __launch_bounds__(256) ldlq_feedback_kernel(float *__restrict__ ACC,
+                                                            const float *__restrict__ M, int64_t n,
+                                                            int64_t cols, int64_t j,
+                                                            const float *__restrict__ E,
+                                                            const float *__restrict__ R,
+                                                            float *__restrict__ U) {
+    __shared__ float Ms[16][kFbRows];
+    const int64_t above = 16 * j;
+    const int64_t r0 = (int64_t)blockIdx.y * kFbRows;
+    for (int e = threadIdx.x; e < 16 * kFbRows; e += blockDim.x) {
+        const int ii = e / kFbRows, rr = e % kFbRows;
+        Ms[ii][rr] = (r0 + rr < above) ? M[(above + ii) * n + r0 + rr] : 0.0f;
+    }
+    __syncthreads();
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols)
+        return;
+    float e[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ii++)
+        e[ii] = E[ii * cols + c];
+    const int64_t span_lo = above - 16;
+    for (int rr = 0; rr < kFbRows; rr++) {
+        const int64_t r = r0 + rr;
+        if (r >= above)
+            break;
+        float a = ACC[r * cols + c];
+#pragma unroll
+        for (int ii = 15; ii >= 0; ii--)
+            a = __fmaf_rn(Ms[ii][rr], e[ii], a);
+        if (r >= span_lo)
+            U[(r - span_lo) * cols + c] = __fadd_rn(R[r * cols + c], a);
+        else
+            ACC[r * cols + c] = a;
+    }
+}
+
+}  // namespace
+
+exl3_status run_block_ldl(const BlockLdlLaunch &p, cudaStream_t s) {
+    const int64_t n = p.n;
+    exl3_status st;
+    diag_delta_kernel<<<1, 1024, 0, s>>>(p.H, n, p.sigma_reg, p.delta);
+    note_launch();
+    for (int a = 0; a <= p.max_retries; a++) {
+        const int ix = (int)((n + 255) / 256 < 64 ? (n + 255) / 256 : 64);
+        chol_init_kernel<<<dim3(ix, (unsigned)n), 256, 0, s>>>(p.H, p.A, n, a, p.delta, p.flag);
+        note_launch();
+        for (int64_t p0 = 0; p0 < n; p0 += 16) {
+            const int64_t below = n - p0 - 16;
+            const unsigned gp = below > 0 ? (unsigned)((below + 255) / 256) : 1u;
+            chol_panel_kernel<<<gp, 256, 0, s>>>(p.A, p.LD + (p0 / 16) * 256, n, p0, p.flag);
+            note_launch();
+            if (below > 0) {
+                const unsigned T = (unsigned)((below + kUpdTile - 1) / kUpdTile);
+                chol_update_kernel<<<dim3(T, T), 256, 0, s>>>(p.A, n, p0);
+                note_launch();
+            }
+        }
+        if ((st = cuda_check(cudaGetLastError(), "cholesky launch")) != EXL3_OK) return st;
+        int failed = 0;
+        if ((st = cuda_check(cudaMemcpyAsync(&failed, p.flag, sizeof(int), cudaMemcpyDeviceToHost, s),
+                             "pivot flag copy")) != EXL3_OK)
+            return st;
+        if ((st = cuda_check(cudaStreamSynchronize(s), "pivot flag wait")) != EXL3_OK) return st;
+        if (!failed) {
+            if ((st = cuda_check(cudaMemsetAsync(p.M, 0, (size_t)n * n * sizeof(float), s),
+                                 "M clear")) != EXL3_OK)
+                return st;
+            if (n > 16) {
+                const unsigned gx = (unsigned)((n - 16 + 255) / 256);
+                ldl_fold_kernel<<<dim3(gx, (unsigned)(n / 16 - 1)), 256, 0, s>>>(p.A, p.LD, n, p.M);
+                note_launch();
+            }
+            if (p.retries_out)
+                *p.retries_out = a;
+            return cuda_check(cudaGetLastError(), "fold launch");
+        }
+    }
+    if (p.retries_out)
+        *p.retries_out = -1;
+    return set_error(EXL3_ERR_NUMERIC, "H is not positive definite after %d damping retries",
+                     p.max_retries);
+}
+
+exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s) {
+    const int64_t n = p.rows, cols = p.cols;
+    const int64_t B = n / 16, TC = cols / 16;
+    const int64_t words = 8 * (int64_t)p.K;          // uint32 words per tile
+    const float inv = 1.0f / p.scale;
+    exl3_status st;
+    if ((st = cuda_check(cudaMemsetAsync(p.acc, 0, (size_t)n * cols * sizeof(float), s),
+                         "feedback clear")) != EXL3_OK)
+        return st;
+    ldlq_first_target_kernel<<<(unsigned)((16 * cols + 255) / 256), 256, 0, s>>>(p.R, cols,
+                                                                                  16 * (B - 1), p.U);
+    note_launch();
+    const int64_t need = TC * (p.K == 1 ? 2 : 1);
+    for (int64_t j = B - 1; j >= 0; j--) {
+        EncodeLaunch el{};
+        el.Y = p.U;
+        el.rows = 16;
+        el.cols = cols;
+        el.K = p.K;
+        el.T = 256;
+        el.row_tiles = 0;
+        el.inv_scale = inv;
+        el.inv_scale_dev = nullptr;
+        el.codes = p.codes + j * TC * words;
+        el.tile_cost = nullptr;
+        el.scratch = p.enc;
+        el.grid = (int)(p.grid < need ? p.grid : need);
+        if ((st = launch_encode(el, s)) != EXL3_OK) return st;
+        ldlq_error_kernel<<<(unsigned)TC, 256, 0, s>>>(p.codes + j * TC * words, p.K, p.R, cols,
+                                                        16 * j, p.scale, p.E, p.Q);
+        note_launch();
+        if (j > 0) {
+            const dim3 g((unsigned)((cols + 255) / 256), (unsigned)((16 * j + kFbRows - 1) / kFbRows));
+            ldlq_feedback_kernel<<<g, 256, 0, s>>>(p.acc, p.M, n, cols, j, p.E, p.R, p.U);
+            note_launch();
+        }
+        if ((st = cuda_check(cudaGetLastError(), "ldlq launch")) != EXL3_OK) return st;
+    }
+    return EXL3_OK;
+}
+
+}  // namespace exl3

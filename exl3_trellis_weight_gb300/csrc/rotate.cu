@@ -44,30 +44,6 @@ __device__ __forceinline__ float load_elem(const void *p, int dt, size_t idx) {
     return reinterpret_cast<const float *>(p)[idx];
 }
 
-// 16-bit window of a tile's circular code stream ending with the last bit of
-// code i (stream bits [(i+1)K - 16, (i+1)K) modulo 256K, MSB first).
-template <int K>
-__device__ __forceinline__ uint32_t window_state(const uint32_t *w, int i) {
-    constexpr int NB = 256 * K;
-    constexpr int NW = 8 * K;
-    int p = (i + 1) * K - 16;
-    if (p < 0)
-        p += NB;
-    const int wi = p >> 5;
-    const int wj = (wi + 1 == NW) ? 0 : wi + 1;
-    const unsigned long long cat = ((unsigned long long)w[wi] << 32) | w[wj];
-    return (uint32_t)(cat >> (48 - (p & 31))) & 0xFFFFu;
-}
-
-__device__ __forceinline__ uint32_t window_state_k(const uint32_t *w, int i, int K) {
-    switch (K) {
-    case 1: return window_state<1>(w, i);
-    case 2: return window_state<2>(w, i);
-    case 3: return window_state<3>(w, i);
-    default: return window_state<4>(w, i);
-    }
-}
-
 __global__ void __launch_bounds__(kRotThreads) rotate_kernel(const RotateLaunch a) {
     extern __shared__ __align__(16) unsigned char smem[];
     float *tile = reinterpret_cast<float *>(smem);                  // [128][kPitch]

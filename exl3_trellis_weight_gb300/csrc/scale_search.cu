@@ -134,15 +134,7 @@ __global__ void row_error_kernel(const uint32_t *__restrict__ codes, int K, cons
         cw[threadIdx.x] = codes[(size_t)row * NW + threadIdx.x];
     __syncthreads();
     const int i = threadIdx.x;
-    // 16-bit window of the circular 256K-bit stream ending with code i
-    int p = (i + 1) * K - 16;
-    if (p < 0)
-        p += 256 * K;
-    const int wi = p >> 5;
-    const int wj = (wi + 1 == NW) ? 0 : wi + 1;
-    const unsigned long long cat = ((unsigned long long)cw[wi] << 32) | cw[wj];
-    const uint32_t st = (uint32_t)(cat >> (48 - (p & 31))) & 0xFFFFu;
-    yh[i] = __fmul_rn(mul1_value(st), s_per_g[gi]);
+    yh[i] = __fmul_rn(mul1_value(window_state_k(cw, i, K)), s_per_g[gi]);
     __syncthreads();
     if (threadIdx.x == 0) {
         double acc = 0.0;

@@ -15,6 +15,16 @@ heads, 8 KV heads and a 12288-wide MLP):
                          target standard deviation; t = z / sqrt(chi2_nu / nu)
                          with chi2_nu a sum of nu squared standard normals.
   * ``signs``         -- fp32 vector of independent +-1 with probability 1/2.
+  * ``spd_hessian``   -- fp64 [n, n] stand-in for a harvested input Hessian:
+                         H = X^T X / N + 0.01 mean(diag) I over N = 2n synthetic
+                         activation rows; along the channel axis X is an AR(1)
+                         process (neighbouring channels correlated with rho) and
+                         each channel is scaled by exp(0.5 z), z ~ N(0, 1)
+                         (a spread of channel magnitudes like real activations).
+  * ``spectral_hessian`` -- fp64 symmetric Q diag(eigs) Q^T with Q orthogonal
+                         from the QR factorisation of a seeded Gaussian matrix;
+                         used to place the smallest eigenvalue exactly (e.g.
+                         indefinite matrices for the damping retries).
 """
 from __future__ import annotations
 
@@ -111,3 +121,29 @@ def workload(name: str):
         W = linear_bf16(4096, 4096, 0, 0.02)
         return [("gss4096", W, *sign_pair(4096, 4096, 0), 2)]
     raise KeyError(name)
+
+
+def spd_hessian(n: int, seed: int = 0, rho: float = 0.9, n_samples: int | None = None,
+                damp: float = 0.01) -> torch.Tensor:
+    g = _gen(seed)
+    N = n_samples or 2 * n
+    z = torch.randn(N, n, generator=g, dtype=torch.float64)
+    x = torch.empty_like(z)
+    x[:, 0] = z[:, 0]
+    c = math.sqrt(1.0 - rho * rho)
+    for k in range(1, n):
+        x[:, k] = rho * x[:, k - 1] + c * z[:, k]
+    x *= torch.exp(0.5 * torch.randn(n, generator=g, dtype=torch.float64))
+    H = x.T @ x / N
+    H = 0.5 * (H + H.T)
+    H += damp * torch.diagonal(H).mean() * torch.eye(n, dtype=torch.float64)
+    return H
+
+
+def spectral_hessian(n: int, eigs, seed: int = 0) -> torch.Tensor:
+    g = _gen(seed)
+    q, r = torch.linalg.qr(torch.randn(n, n, generator=g, dtype=torch.float64))
+    q = q * torch.sign(torch.diagonal(r))
+    lam = torch.as_tensor(eigs, dtype=torch.float64)
+    H = (q * lam) @ q.T
+    return 0.5 * (H + H.T)

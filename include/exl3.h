@@ -19,7 +19,8 @@
  *     elements are taken row-major.  Codes are uint16 [rows/16][cols/16][16*K]
  *     (see exl3_encode_tiles for the bit layout).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
- *     is enqueued on it; no entry point synchronises the host with the device.
+ *     is enqueued on it; no entry point synchronises the host with the device,
+ *     except exl3_block_ldl, whose damping retries depend on a device result.
  *   - The library allocates no device memory.  Scratch comes from the caller's
  *     workspace `ws` (device, 256-byte aligned) of `ws_bytes` bytes, sized with
  *     the matching *_workspace_bytes query.  The workspace must not be used by
@@ -56,7 +57,8 @@ typedef enum {
     EXL3_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad bracket */
     EXL3_ERR_UNSUPPORTED = 2,  /* K outside the built set, dims not multiples of 16/128 */
     EXL3_ERR_WORKSPACE = 3,    /* ws_bytes below the minimum for this call */
-    EXL3_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+    EXL3_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    EXL3_ERR_NUMERIC = 5       /* the input has no factorisation (exl3_block_ldl) */
 } exl3_status;
 
 typedef enum { EXL3_F32 = 0, EXL3_BF16 = 1 } exl3_dtype;
@@ -249,6 +251,66 @@ EXL3_API exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int6
                                        const float *su, const float *sv, int K, double *g_out,
                                        float *scale_out, double *history_out, void *ws,
                                        size_t ws_bytes, void *stream);
+
+/*
+ * Block LDL factorisation of a Hessian (README item 3: blockwise Cholesky/LDL,
+ * the inverse of the 16x16 block diagonal folded in, retry-only damping of
+ * 2 sigma_reg mean(diag H) up to 10 times).
+ *   H = L L^T (binary64 Cholesky in the textbook order: each entry
+ *   H[i][j] - sum_{k<j} L[i][k] L[j][k], k ascending, one rounded product and
+ *   one rounded difference per term; sqrt / divide correctly rounded).  With
+ *   Lambda = blockdiag of L's 16x16 diagonal blocks, M = L Lambda^-1 is unit
+ *   block-lower-triangular and H = M (Lambda Lambda^T) M^T.
+ *   Attempt a = 0, 1, ..., max_retries factors H + a * delta * I,
+ *   delta = (2 sigma_reg) * (ascending sum of diag H / n); the first attempt
+ *   whose pivots are all > 0 is kept.
+ *   H (device) double [n, n] row-major, symmetric: only the lower triangle is
+ *     read; n a multiple of 16 in [16, 32768].
+ *   sigma_reg >= 0 and finite (0.01 in the README's damping); max_retries in
+ *     [0, 100] (10 in the README).
+ *   M (device, 16-byte aligned) float [n, n] out: fl32 of M's strictly lower
+ *     block part (the entries below the 16x16 diagonal blocks); the diagonal
+ *     blocks (identity) and everything above them are written as 0.  Each
+ *     entry M[i][16b+c] = fl32(sum_{k=c..15} L[i][16b+k] X[k][c]) with X the
+ *     inverse of diagonal block b by forward substitution.
+ *   retries_out (host) int or NULL: the number of retries used, -1 on failure.
+ *   ws: exl3_block_ldl_workspace_bytes(n).
+ * Returns EXL3_ERR_NUMERIC when every attempt has a non-positive pivot (M is
+ * then not written).  The call synchronises `stream` once per attempt: it
+ * reads the pivot flag back to decide whether to retry.
+ */
+EXL3_API size_t exl3_block_ldl_workspace_bytes(int64_t n);
+EXL3_API exl3_status exl3_block_ldl(const double *H, int64_t n, double sigma_reg, int max_retries,
+                                    float *M, int *retries_out, void *ws, size_t ws_bytes,
+                                    void *stream);
+
+/*
+ * LDLQ: trellis-code the 16-row spans of R bottom-up with error feedback
+ * (README item 3: one-sided LDLQ error feedback, the tile encoder as the
+ * callback on each span).  With E = fl32(R - Q) for the spans already coded
+ * (Q = fl32(v * scale)), span b (rows 16b .. 16b+15) is coded from the
+ * targets U_b = fl32(R_b + acc_b), where acc_b[r][c] is the binary32 chain
+ * acc = fmaf(M[i][16b + r], E[i][c], acc) over i = rows-1 down to 16(b+1)
+ * (starting from 0), i.e. the correction sum_{i below the span} M[i, span]^T E_i
+ * that minimises the Hessian-weighted error tr(E^T H E) span by span.
+ * Codes come from fl32(U * fl32(1 / scale)), as in exl3_encode_tiles.
+ *   R (device) float [rows, cols]: rotated weights with the input channels (the
+ *     Hessian's index) down the rows; rows and cols multiples of 16.
+ *   M (device) float [rows, rows]: from exl3_block_ldl (only the strictly
+ *     lower block part is read).
+ *   K in {1, 2, 3, 4}; scale > 0 and finite (e.g. fl32(g * sigma_R)).
+ *   codes (device) uint16 [rows/16, cols/16, 16K] out, the layout of
+ *     exl3_encode_tiles; Q (device) float [rows, cols] out or NULL: the
+ *     reconstruction fl32(v * scale) of every span.
+ *   ws: exl3_ldlq_workspace_bytes(rows, cols, K); a smaller workspace (at least
+ *     the K's encode minimum on top of the fixed part) runs fewer encode blocks.
+ * The spans are coded one after another (each depends on the errors of the
+ * ones below it): rows / 16 encode launches of cols / 16 tiles each.
+ */
+EXL3_API size_t exl3_ldlq_workspace_bytes(int64_t rows, int64_t cols, int K);
+EXL3_API exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M, int K,
+                               float scale, uint16_t *codes, float *Q, void *ws, size_t ws_bytes,
+                               void *stream);
 
 /*
  * exl3_encode_tiles without a workspace, for callers that cannot allocate

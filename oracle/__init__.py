@@ -77,6 +77,13 @@ def _load():
         L.ora_tile_sumsq.argtypes = [P, P, i64, i64, P]
         L.ora_tree_sum.argtypes = [P, i64]
         L.ora_tree_sum.restype = ctypes.c_double
+        f64 = ctypes.c_double
+        L.ora_cholesky.argtypes = [P, i64, f64, P]
+        L.ora_cholesky.restype = i32
+        L.ora_cholesky_damped.argtypes = [P, i64, f64, i32, P]
+        L.ora_cholesky_damped.restype = i32
+        L.ora_block_fold.argtypes = [P, i64, P]
+        L.ora_ldlq_feedback.argtypes = [P, P, i64, i64, i64, P]
         _lib = L
         return L
 

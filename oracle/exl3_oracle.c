@@ -28,6 +28,12 @@
  *           order H_l -> x su -> H_r -> x sv.
  *   [Qual]  item 10, "Single-Layer Quantization & Distortion Metrics":
  *           reconstruction MSE.
+ *   [LDL]   item 3, "Block LDLQ Decomposition & Preprocessing": blockwise
+ *           Cholesky/LDL with the block-diagonal inverse folded in
+ *           (M = L * blockdiag(L_bb)^-1), damping retries of
+ *           2 * sigma_reg * mean(diag H) up to 10 times, bottom-up error
+ *           feedback from the strictly lower part of M into the targets of the
+ *           rows not yet quantised.
  *
  * Readings fixed where the pages are silent (each also listed in the design
  * notes of the repository):
@@ -458,4 +464,118 @@ double ora_tree_sum(const double *v, int64_t n)
     double r = a[0];
     free(a);
     return r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block LDL and LDLQ error feedback  [LDL]                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Textbook Cholesky H = L L^T in binary64.  Only the lower triangle of H
+ * (row-major n x n) is read; L is written row-major with its upper triangle
+ * set to zero.  Column by column, each entry is
+ *     acc = H[i][j];  for k = 0 .. j-1:  acc = acc - L[i][k] * L[j][k]
+ * (one rounded product and one rounded difference per term, ascending k),
+ * then L[j][j] = sqrt(acc) and L[i][j] = acc / L[j][j] for i > j.  diag_add
+ * is added to every diagonal entry of H first (0 for none).  Returns 0, or
+ * j + 1 for the first column whose pivot acc is not > 0. */
+int ora_cholesky(const double *H, int64_t n, double diag_add, double *L)
+{
+    memset(L, 0, sizeof(double) * (size_t)n * (size_t)n);
+    for (int64_t j = 0; j < n; j++) {
+        double acc = H[j * n + j] + diag_add;
+        for (int64_t k = 0; k < j; k++)
+            acc = acc - L[j * n + k] * L[j * n + k];
+        if (!(acc > 0.0))
+            return (int)(j + 1);
+        const double d = sqrt(acc);
+        L[j * n + j] = d;
+        for (int64_t i = j + 1; i < n; i++) {
+            double a = H[i * n + j];
+            for (int64_t k = 0; k < j; k++)
+                a = a - L[i * n + k] * L[j * n + k];
+            L[i * n + j] = a / d;
+        }
+    }
+    return 0;
+}
+
+/* Retry schedule: attempt a = 0, 1, ..., max_retries factors
+ * H + a * delta * I with delta = (2 * sigma_reg) * mean, mean = (sum of the
+ * diagonal in ascending order) / n, and the diagonal addend a * delta rounded
+ * once.  Returns the number of retries used (0 = undamped), or -1 when every
+ * attempt failed. */
+int ora_cholesky_damped(const double *H, int64_t n, double sigma_reg, int max_retries, double *L)
+{
+    double sum = 0.0;
+    for (int64_t j = 0; j < n; j++)
+        sum = sum + H[j * n + j];
+    const double delta = (2.0 * sigma_reg) * (sum / (double)n);
+    for (int a = 0; a <= max_retries; a++) {
+        if (ora_cholesky(H, n, (double)a * delta, L) == 0)
+            return a;
+    }
+    return -1;
+}
+
+/* Inverse of a 16x16 lower-triangular block (row stride ld) by forward
+ * substitution, binary64:  X[c][c] = 1 / B[c][c];  for r > c:
+ *     acc = 0;  for k = c .. r-1:  acc = acc + B[r][k] * X[k][c];
+ *     X[r][c] = -acc / B[r][r]. */
+static void lower16_inverse(const double *B, int64_t ld, double X[16][16])
+{
+    for (int r = 0; r < 16; r++)
+        for (int c = 0; c < 16; c++)
+            X[r][c] = 0.0;
+    for (int c = 0; c < 16; c++) {
+        X[c][c] = 1.0 / B[c * ld + c];
+        for (int r = c + 1; r < 16; r++) {
+            double acc = 0.0;
+            for (int k = c; k < r; k++)
+                acc = acc + B[r * ld + k] * X[k][c];
+            X[r][c] = -acc / B[r * ld + r];
+        }
+    }
+}
+
+/* Block LDL fold: with Lambda = blockdiag of the 16x16 diagonal blocks of
+ * L, M = L * Lambda^-1 is unit block-lower-triangular and
+ * H = M * (Lambda Lambda^T) * M^T.  Writes fl32 of the strictly lower block
+ * part of M (row-major n x n):  for block column b, rows i >= 16 (b + 1),
+ *     M[i][16b + c] = sum_{k = c .. 15} L[i][16b + k] * X[k][c]
+ * (ascending k, binary64, X = inverse of the diagonal block); the diagonal
+ * blocks (identity) and everything above them are written as zero. */
+void ora_block_fold(const double *L, int64_t n, float *M)
+{
+    memset(M, 0, sizeof(float) * (size_t)n * (size_t)n);
+    for (int64_t b = 0; b < n / 16; b++) {
+        double X[16][16];
+        lower16_inverse(L + (16 * b) * n + 16 * b, n, X);
+        for (int64_t i = 16 * (b + 1); i < n; i++) {
+            for (int c = 0; c < 16; c++) {
+                double acc = 0.0;
+                for (int k = c; k < 16; k++)
+                    acc = acc + L[i * n + 16 * b + k] * X[k][c];
+                M[i * n + 16 * b + c] = (float)acc;
+            }
+        }
+    }
+}
+
+/* Error feedback of one quantised block-row j (rows 16j .. 16j+15, errors
+ * E[16][cols] = fl32(R - Q) of that block-row) into the accumulated target
+ * corrections acc[r][c] of every row r < 16 j:
+ *     for i = 16 j + 15 down to 16 j:  acc[r][c] = fmaf(M[i][r], E[i - 16 j][c], acc[r][c])
+ * Rows are quantised bottom-up, so over the whole sweep each correction is
+ * the fp32 fused-multiply-add chain over i = n-1 down to 16 (b + 1). */
+void ora_ldlq_feedback(float *acc, const float *M, int64_t n, int64_t cols, int64_t j,
+                       const float *E)
+{
+    for (int64_t r = 0; r < 16 * j; r++) {
+        for (int64_t c = 0; c < cols; c++) {
+            float a = acc[r * cols + c];
+            for (int64_t i = 16 * j + 15; i >= 16 * j; i--)
+                a = fmaf(M[i * n + r], E[(i - 16 * j) * cols + c], a);
+            acc[r * cols + c] = a;
+        }
+    }
 }

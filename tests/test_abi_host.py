@@ -120,6 +120,34 @@ def test_rotate_and_quantize_reject_bad_arguments(ex):
     assert sc(32768, 128, 2) == 2        # beyond the 32736-row limit
 
 
+def test_ldl_and_ldlq_reject_bad_arguments(ex):
+    L = ex.lib()
+    wl = ex.block_ldl_workspace_bytes(64)
+    ldl = lambda n=64, H=FAKE, M=FAKE, sig=0.01, r=10, w=wl: L.exl3_block_ldl(
+        H, n, ctypes.c_double(sig), r, M, None, FAKE, w, None)
+    assert ldl(n=40) == 2 and ldl(n=0) == 2 and ldl(n=32784) == 2
+    assert ldl(H=None) == 1
+    assert ldl(M=ctypes.c_void_p(0x10000004)) == 1          # M must be 16-byte aligned
+    assert ldl(sig=-1.0) == 1 and ldl(sig=float("inf")) == 1
+    assert ldl(r=-1) == 1 and ldl(r=101) == 1
+    assert ldl(w=wl - 1) == 3
+    assert ex.block_ldl_workspace_bytes(64) >= 64 * 64 * 8
+    assert ex.block_ldl_workspace_bytes(40) == 0
+    wq = ex.ldlq_workspace_bytes(64, 128, 2)
+    lq = lambda rows=64, cols=128, K=2, s=1.0, w=wq, codes=FAKE: L.exl3_ldlq(
+        FAKE, rows, cols, FAKE, K, ctypes.c_float(s), codes, None, FAKE, w, None)
+    assert lq(rows=40) == 2 and lq(cols=8) == 2
+    assert lq(K=5) == 2
+    assert lq(s=0.0) == 1 and lq(s=float("nan")) == 1
+    assert lq(codes=None) == 1
+    assert lq(w=64 * 128 * 4) == 3
+    assert ex.ldlq_workspace_bytes(64, 128, 0) == 0
+    # K=1 needs two encode blocks (one cluster)
+    w1 = ex.ldlq_workspace_bytes(64, 128, 1)
+    fixed = w1 - (w1 - 64 * 128 * 4) // ex.encode_workspace_min_bytes(2) * ex.encode_workspace_min_bytes(2)
+    assert lq(K=1, w=fixed + ex.encode_workspace_min_bytes(2)) == 3
+
+
 def test_workspace_queries_scale_with_work(ex):
     a = ex.encode_workspace_bytes(10, 2)
     b = ex.encode_workspace_bytes(100000, 2)

@@ -427,3 +427,106 @@ def test_scale_search_full_size_properties(ex):
     S = ss.sample_tiles(oracle.tile_sumsq(R), 256, 256)
     f = ss.subset_mse(R, S, K, g, oracle.rms(R))
     assert f == min(fine[:, 1].min(), h[26, 1] if h[26, 0] >= 0 else np.inf)
+
+
+# ---------------------------------------------------------------------------
+# block LDL factorisation and LDLQ error feedback
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,seed", [(16, 1), (48, 2), (256, 3), (1024, 4)])
+def test_block_ldl_matches_oracle(ex, n, seed):
+    from oracle import ldlq as OL
+    H = inputs.spd_hessian(n, seed)
+    M, a = ex.block_ldl(H.to(DEV))
+    Mo, ao, _ = OL.block_ldl(H.numpy())
+    assert a == ao == 0
+    assert np.array_equal(M.cpu().numpy(), Mo)
+
+
+def test_block_ldl_damping_retries_and_failure(ex):
+    from oracle import ldlq as OL
+    n = 64
+    eigs = np.linspace(0.5, 2.0, n)
+    for need in (1, 3):
+        e = eigs.copy()
+        e[0] = -(need - 0.5) * 2 * 0.01 * e.mean()    # half a damping step short
+        e[0] = -(need - 0.5) * 2 * 0.01 * e.mean()    # of `need` retries
+        H = inputs.spectral_hessian(n, e, seed=5)
+        M, a = ex.block_ldl(H.to(DEV))
+        Mo, ao, _ = OL.block_ldl(H.numpy())
+        assert a == ao == need
+        assert np.array_equal(M.cpu().numpy(), Mo)
+    e = eigs.copy()
+    e[0] = -1.0
+    H = inputs.spectral_hessian(n, e, seed=6)
+    with pytest.raises(ex.Exl3Error) as err:
+        ex.block_ldl(H.to(DEV))
+    assert err.value.status == 5
+    # the library stays usable after the failure
+    M, a = ex.block_ldl(inputs.spd_hessian(n, 1).to(DEV))
+    assert a == 0
+
+
+@pytest.mark.parametrize("n,cols,K,seed", [(256, 256, 2, 31), (128, 512, 3, 32), (192, 64, 4, 33),
+                                           (128, 128, 1, 34), (32, 16, 2, 35), (512, 1024, 2, 36)])
+def test_ldlq_matches_oracle(ex, n, cols, K, seed):
+    from oracle import ldlq as OL
+    H = inputs.spd_hessian(n, seed, rho=0.95)
+    Mo, _, _ = OL.block_ldl(H.numpy())
+    R = inputs.iid_f32(n, cols, seed + 100)
+    s = float(np.float32(oracle.rms(R.numpy())))
+    M, _ = ex.block_ldl(H.to(DEV))
+    res = ex.ldlq(R.to(DEV), M, K, s)
+    torch.cuda.synchronize()
+    ref = OL.ldlq(R.numpy(), Mo, K, s)
+    assert np.array_equal(res["codes"].cpu().numpy().view(np.uint16), ref["codes"])
+    assert np.array_equal(res["Q"].cpu().numpy(), ref["Q"])
+
+
+def test_ldlq_small_workspace_and_no_q(ex):
+    from oracle import ldlq as OL
+    n, cols, K = 96, 256, 2
+    H = inputs.spd_hessian(n, 41, rho=0.95)
+    Mo, _, _ = OL.block_ldl(H.numpy())
+    R = inputs.iid_f32(n, cols, 42)
+    s = 0.75
+    M, _ = ex.block_ldl(H.to(DEV))
+    fixed = ex.ldlq_workspace_bytes(n, cols, K) - 16 * ex.encode_workspace_min_bytes(K)
+    ws = torch.empty(fixed + ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
+    res = ex.ldlq(R.to(DEV), M, K, s, want_q=False, ws=ws)
+    torch.cuda.synchronize()
+    ref = OL.ldlq(R.numpy(), Mo, K, s)
+    assert res["Q"] is None
+    assert np.array_equal(res["codes"].cpu().numpy().view(np.uint16), ref["codes"])
+
+
+def test_ldlq_full_size_properties(ex):
+    """4096 x 4096 K=2 with a 4096-channel synthetic Hessian: the factor
+    block-diagonalises H, the bottom span is plain quantisation (oracle), and
+    the feedback lowers the Hessian-weighted error against plain coding."""
+    from oracle import ldlq as OL
+    n, cols, K = 4096, 4096, 2
+    H = inputs.spd_hessian(n, 50, rho=0.95).to(DEV)
+    M, a = ex.block_ldl(H)
+    assert a == 0
+    U = M.double() + torch.eye(n, dtype=torch.float64, device=DEV)
+    Y = torch.linalg.solve_triangular(U, H, upper=False)
+    Z = torch.linalg.solve_triangular(U, Y.T.contiguous(), upper=False)   # U^-1 H U^-T
+    blk = torch.zeros(n, n, dtype=torch.bool, device=DEV)
+    for b in range(n // 16):
+        blk[16 * b:16 * b + 16, 16 * b:16 * b + 16] = True
+    assert Z[~blk].abs().max().item() <= 1e-4 * Z[blk].abs().max().item()
+    R = inputs.iid_f32(n, cols, 51)
+    s = float(np.float32(oracle.rms(R.numpy())))
+    Rd = R.to(DEV)
+    res = ex.ldlq(Rd, M, K, s)
+    torch.cuda.synchronize()
+    bottom = res["codes"][-1:].cpu().numpy().view(np.uint16).reshape(-1, 16 * K)
+    want, _ = _oracle_codes(R.numpy()[n - 16:], K, float(np.float32(1.0) / np.float32(s)))
+    assert np.array_equal(bottom, want)
+    plain = ex.ldlq(Rd, torch.zeros_like(M), K, s)
+    E1 = (Rd - res["Q"]).double()
+    E0 = (Rd - plain["Q"]).double()
+    l1 = ((H @ E1) * E1).sum().item()
+    l0 = ((H @ E0) * E0).sum().item()
+    assert l1 < 0.8 * l0
