@@ -438,6 +438,28 @@ def run_ours(args):
                        "encode_launches": lq_enc_n // len(lq_ms)}
         del ws_q, codes_q, R, M, Hd
 
+        # output-channel regularisation of the same weight (synthetic Hessian diagonal)
+        h_d = inputs.hessian_diag(rows, 52).to(dev)
+        W_o = torch.empty(rows, cols, dtype=torch.float32, device=dev)
+        ws_r = torch.empty(ex.regularize_workspace_bytes(rows, cols), dtype=torch.uint8, device=dev)
+        rr = ex.regularize(W, h_d, sv, W_out=W_o, ws=ws_r)
+        torch.cuda.synchronize(dev)
+        rg_ms = []
+        for _ in range(5):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rr = ex.regularize(W, h_d, sv, W_out=W_o, ws=ws_r)
+            b.record(stream)
+            b.synchronize()
+            rg_ms.append(a.elapsed_time(b))
+        rg_avg = sum(rg_ms) / len(rg_ms)
+        rg_bytes = rows * cols * (2 * W.element_size() + 4)      # two reads of W, one fp32 write
+        aux["regularize"] = {"ms": rg_avg, "GBps": rg_bytes / (rg_avg / 1e3) / 1e9,
+                             "bytes": rg_bytes, "applied": bool(rr["info"][1].item()),
+                             "skew": float(rr["info"][0].item())}
+        del W_o, ws_r, h_d
+
     # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:

@@ -89,10 +89,13 @@ def lib():
         L.exl3_ldlq_workspace_bytes.argtypes = [i64, i64, i32]
         L.exl3_ldlq_workspace_bytes.restype = sz
         L.exl3_ldlq.argtypes = [P, i64, i64, P, i32, f32, P, P, P, sz, P]
+        L.exl3_regularize_workspace_bytes.argtypes = [i64, i64]
+        L.exl3_regularize_workspace_bytes.restype = sz
+        L.exl3_regularize.argtypes = [P, i32, i64, i64, P, P, i32, P, P, P, P, sz, P]
         L.exl3_profile_enable.argtypes = [i32]
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
-        for name in ("exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
+        for name in ("exl3_regularize", "exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
         _lib = L
@@ -355,6 +358,29 @@ def ldlq(R, M, K: int, scale: float, want_q: bool = True, codes=None, ws=None):
     _check(lib().exl3_ldlq(_ptr(R), rows, cols, _ptr(M), K, ctypes.c_float(scale), _ptr(codes),
                            _ptr(Q), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
     return dict(codes=codes, Q=Q)
+
+
+def regularize_workspace_bytes(rows: int, cols: int) -> int:
+    return int(lib().exl3_regularize_workspace_bytes(rows, cols))
+
+
+def regularize(W, h, sv, apply_out: int = -1, W_out=None, ws=None):
+    """exl3_regularize: output-channel normalisation with the skew heuristic.
+    Returns dict(W_out fp32 [rows, cols], sv_out fp32 [cols],
+    info fp64 [4] = (skew, applied, zeros, global rms))."""
+    torch = _torch()
+    _need_cuda(W, h, sv, W_out)
+    rows, cols = W.shape
+    dev = W.device
+    if W_out is None:
+        W_out = torch.empty(rows, cols, dtype=torch.float32, device=dev)
+    sv_out = torch.empty(cols, dtype=torch.float32, device=dev)
+    info = torch.empty(4, dtype=torch.float64, device=dev)
+    ws = _workspace(regularize_workspace_bytes(rows, cols), dev, ws)
+    _check(lib().exl3_regularize(_ptr(W), _dt(W), rows, cols, _ptr(h), _ptr(sv), int(apply_out),
+                                 _ptr(W_out), _ptr(sv_out), _ptr(info), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(dev)))
+    return dict(W_out=W_out, sv_out=sv_out, info=info)
 
 
 def gss_scale(W, su, sv, K: int, lo: float = 0.5, hi: float = 2.0, n_eval: int = 12,

@@ -848,6 +848,74 @@ exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M
     return run_ldlq(l, (cudaStream_t)stream);
 }
 
+// ---- output-channel regularisation ----------------------------------------------
+
+static size_t regularize_carve(void *ws, int64_t rows, int64_t cols, RegularizeLaunch *out) {
+    Carver c(ws);
+    RegularizeLaunch r{};
+    r.part = (double *)c.take((size_t)32 * cols * sizeof(double));
+    r.S = (double *)c.take((size_t)cols * sizeof(double));
+    r.tree_scr = (double *)c.take(tree_scratch_doubles(rows > cols ? rows : cols) * sizeof(double));
+    r.total = (double *)c.take(sizeof(double));
+    r.sortbuf = (double *)c.take((size_t)regularize_sort_len(rows) * sizeof(double));
+    r.hsum = (double *)c.take(2 * sizeof(double));
+    r.info = (double *)c.take(4 * sizeof(double));
+    r.g_rms = (float *)c.take(sizeof(float));
+    r.scale = (float *)c.take((size_t)cols * sizeof(float));
+    if (out)
+        *out = r;
+    return c.off;
+}
+
+static bool reg_dims_ok(int64_t rows, int64_t cols) {
+    return rows >= 1 && cols >= 1 && rows <= 65536 && cols <= (int64_t)1 << 24;
+}
+
+size_t exl3_regularize_workspace_bytes(int64_t rows, int64_t cols) {
+    if (!reg_dims_ok(rows, cols))
+        return 0;
+    return regularize_carve(nullptr, rows, cols, nullptr);
+}
+
+exl3_status exl3_regularize(const void *W, int dt, int64_t rows, int64_t cols, const float *h,
+                            const float *sv, int apply_out, float *W_out, float *sv_out,
+                            double *info_out, void *ws, size_t ws_bytes, void *stream) {
+    exl3_status st;
+    if (dt != EXL3_F32 && dt != EXL3_BF16)
+        return set_error(EXL3_ERR_INVALID_ARG, "dt=%d is not EXL3_F32 or EXL3_BF16", dt);
+    if ((st = check_ptr(W, "W", dt == EXL3_BF16 ? 2 : 4)) != EXL3_OK) return st;
+    if (!reg_dims_ok(rows, cols))
+        return set_error(EXL3_ERR_UNSUPPORTED, "rows in [1, 65536] and cols in [1, 2^24] required");
+    if ((st = check_ptr(h, "h", 4)) != EXL3_OK) return st;
+    if ((st = check_ptr(sv, "sv", 4)) != EXL3_OK) return st;
+    if (apply_out < -1 || apply_out > 1)
+        return set_error(EXL3_ERR_INVALID_ARG, "apply_out=%d is not -1, 0 or 1", apply_out);
+    if ((st = check_ptr(W_out, "W_out", 4)) != EXL3_OK) return st;
+    if ((st = check_ptr(sv_out, "sv_out", 4)) != EXL3_OK) return st;
+    if (info_out && !aligned(info_out, 8))
+        return set_error(EXL3_ERR_INVALID_ARG, "info_out is not 8-byte aligned");
+    if (dt == EXL3_BF16 && (const void *)W_out == W)
+        return set_error(EXL3_ERR_INVALID_ARG, "in-place regularisation needs an fp32 W");
+    if (!ws || !aligned(ws, kAlign))
+        return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    const size_t need = regularize_carve(nullptr, rows, cols, nullptr);
+    if (ws_bytes < need)
+        return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes < %zu", ws_bytes, need);
+    RegularizeLaunch r{};
+    regularize_carve(ws, rows, cols, &r);
+    r.W = W;
+    r.dt = dt;
+    r.rows = rows;
+    r.cols = cols;
+    r.h = h;
+    r.sv = sv;
+    r.apply_out = apply_out;
+    r.W_out = W_out;
+    r.sv_out = sv_out;
+    r.info_out = info_out;
+    return run_regularize(r, (cudaStream_t)stream);
+}
+
 void exl3_profile_enable(int on) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     g_prof_on.store(on != 0);

@@ -236,6 +236,30 @@ struct LdlqLaunch {
 };
 exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s);
 
+// output-channel regularisation (regularize.cu)
+struct RegularizeLaunch {
+    const void *W;
+    int dt;
+    int64_t rows, cols;
+    const float *h;         // [rows]
+    const float *sv;        // [cols]
+    int apply_out;          // -1 heuristic, 0 / 1 forced
+    float *W_out;           // [rows, cols]
+    float *sv_out;          // [cols]
+    double *info_out;       // nullable, [4]
+    double *part;           // [32, cols]
+    double *S;              // [cols]
+    double *tree_scr;       // tree_scratch_doubles(max(rows, cols))
+    double *total;          // scalar
+    double *sortbuf;        // [regularize_sort_len(rows)]
+    double *hsum;           // [2]: trees of the top sqrt(h) and of all
+    double *info;           // [4]
+    float *g_rms;           // scalar
+    float *scale;           // [cols]
+};
+int64_t regularize_sort_len(int64_t rows);
+exl3_status run_regularize(const RegularizeLaunch &p, cudaStream_t s);
+
 exl3_status launch_tile_sumsq(const void *x, int x_dt, const float *ref, int64_t rows,
                               int64_t cols, double *tile_sums, cudaStream_t s);
 // tree sum of n doubles; scratch >= tree_scratch_doubles(n) doubles; result -> *out

@@ -64,21 +64,26 @@ __global__ void chol_init_kernel(const double *__restrict__ H, double *__restric
     }
 }
 
-// Panel p0 (columns p0 .. p0+15).  Every block factors the 16x16 diagonal
-// block in shared memory (identically); block 0 stores it to LD (the rows of A
-// inside the diagonal block are left as they are, so no block reads a value
-// another one has overwritten).  Then one row i >= p0 + 16 per thread:
+// Panel p0 (columns p0 .. p0+15), one warp per block so that the rows spread
+// over many SMs (the FP64 units are few per SM).  Every block factors the
+// 16x16 diagonal block in shared memory (identically); block 0 stores it to
+// LD (the rows of A inside the diagonal block are left as they are, so no
+// block reads a value another one has overwritten).  Then one row
+// i >= p0 + 16 per thread:
 // L[i][p0+j] = (A[i][p0+j] - sum_{k<j} L[i][p0+k] L[p0+j][p0+k]) / L[p0+j][p0+j].
-__global__ void __launch_bounds__(256) chol_panel_kernel(double *__restrict__ A, double *__restrict__ LD,
-                                                         int64_t n, int64_t p0, int *flag) {
+constexpr int kPanelThreads = 32;
+
+__global__ void __launch_bounds__(kPanelThreads) chol_panel_kernel(double *__restrict__ A,
+                                                                   double *__restrict__ LD,
+                                                                   int64_t n, int64_t p0, int *flag) {
     __shared__ double D[16][17];
     const int t = threadIdx.x;
-    {
-        const int r = t >> 4, c = t & 15;
+    for (int e = t; e < 256; e += kPanelThreads) {
+        const int r = e >> 4, c = e & 15;
         D[r][c] = (c <= r) ? A[(p0 + r) * n + p0 + c] : 0.0;
     }
     __syncthreads();
-    if (t < 32) {
+    {
         const int r = t & 15;     // lanes 16..31 repeat lanes 0..15 and never store
         for (int j = 0; j < 16; j++) {
             double acc = D[r][j];
@@ -101,8 +106,8 @@ __global__ void __launch_bounds__(256) chol_panel_kernel(double *__restrict__ A,
     }
     __syncthreads();
     if (blockIdx.x == 0) {
-        const int r = t >> 4, c = t & 15;
-        LD[r * 16 + c] = D[r][c];
+        for (int e = t; e < 256; e += kPanelThreads)
+            LD[e] = D[e >> 4][e & 15];
     }
     const int64_t i = p0 + 16 + (int64_t)blockIdx.x * blockDim.x + t;
     if (i >= n)
@@ -302,8 +307,10 @@ exl3_status run_block_ldl(const BlockLdlLaunch &p, cudaStream_t s) {
         note_launch();
         for (int64_t p0 = 0; p0 < n; p0 += 16) {
             const int64_t below = n - p0 - 16;
-            const unsigned gp = below > 0 ? (unsigned)((below + 255) / 256) : 1u;
-            chol_panel_kernel<<<gp, 256, 0, s>>>(p.A, p.LD + (p0 / 16) * 256, n, p0, p.flag);
+            const unsigned gp =
+                below > 0 ? (unsigned)((below + kPanelThreads - 1) / kPanelThreads) : 1u;
+            chol_panel_kernel<<<gp, kPanelThreads, 0, s>>>(p.A, p.LD + (p0 / 16) * 256, n, p0,
+                                                           p.flag);
             note_launch();
             if (below > 0) {
                 const unsigned T = (unsigned)((below + kUpdTile - 1) / kUpdTile);

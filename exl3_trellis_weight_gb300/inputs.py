@@ -21,6 +21,10 @@ heads, 8 KV heads and a 12288-wide MLP):
                          process (neighbouring channels correlated with rho) and
                          each channel is scaled by exp(0.5 z), z ~ N(0, 1)
                          (a spread of channel magnitudes like real activations).
+  * ``hessian_diag``  -- fp32 [n] diagonal of such a Hessian without forming it:
+                         channel energies exp(z) (the squared lognormal channel
+                         scales), sampling noise of N = 2n rows in the normal
+                         approximation of chi2_N / N, plus 1 % of the mean.
   * ``spectral_hessian`` -- fp64 symmetric Q diag(eigs) Q^T with Q orthogonal
                          from the QR factorisation of a seeded Gaussian matrix;
                          used to place the smallest eigenvalue exactly (e.g.
@@ -147,3 +151,12 @@ def spectral_hessian(n: int, eigs, seed: int = 0) -> torch.Tensor:
     lam = torch.as_tensor(eigs, dtype=torch.float64)
     H = (q * lam) @ q.T
     return 0.5 * (H + H.T)
+
+
+def hessian_diag(n: int, seed: int = 0, damp: float = 0.01) -> torch.Tensor:
+    g = _gen(seed)
+    energy = torch.exp(torch.randn(n, generator=g, dtype=torch.float64))
+    noise = 1.0 + math.sqrt(2.0 / (2 * n)) * torch.randn(n, generator=g, dtype=torch.float64)
+    h = energy * noise.clamp_min(0.0)
+    h += damp * h.mean()
+    return h.to(torch.float32)

@@ -3,11 +3,19 @@
     python -m exl3_trellis_weight_gb300.profile_cases encode --K 2 --rows 1216 --cols 256
     python -m exl3_trellis_weight_gb300.profile_cases rotate --rows 4096 --cols 4096
     python -m exl3_trellis_weight_gb300.profile_cases alu-mix
+    python -m exl3_trellis_weight_gb300.profile_cases regularize --rows 4096 --cols 4096
+    python -m exl3_trellis_weight_gb300.profile_cases ldl --rows 4096
+    python -m exl3_trellis_weight_gb300.profile_cases ldlq --rows 1024 --cols 4096 --K 2
 
 encode  : exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1.
 rotate  : exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix.
 alu-mix : build and run microbench/alu_mix.cu (instruction issue rates per SM
           per clock of the kinds the encoder uses).
+regularize : exl3_regularize of a bf16 N(0, 0.02^2) matrix with a synthetic
+          Hessian diagonal (inputs.hessian_diag).
+ldl     : exl3_block_ldl of inputs.spd_hessian(rows) (rho 0.95).
+ldlq    : exl3_ldlq of fp32 N(0, 1) targets with the factor of
+          inputs.spd_hessian(rows), scale 1.
 Each launch case runs --reps launches and synchronises; it prints the wall time.
 """
 from __future__ import annotations
@@ -28,7 +36,7 @@ def main(argv=None) -> int:
     from exl3_trellis_weight_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["encode", "rotate", "alu-mix"])
+    ap.add_argument("case", choices=["encode", "rotate", "alu-mix", "regularize", "ldl", "ldlq"])
     ap.add_argument("--K", type=int, default=2)
     ap.add_argument("--rows", type=int, default=1216)
     ap.add_argument("--cols", type=int, default=256)
@@ -49,6 +57,27 @@ def main(argv=None) -> int:
         ws = torch.empty(ex.encode_workspace_bytes(n, a.K), dtype=torch.uint8, device=dev)
         codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
         fn = lambda: ex.encode_tiles(Y, a.K, 1.0, codes=codes, ws=ws)
+    elif a.case == "regularize":
+        W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
+        h = inputs.hessian_diag(a.rows, 0).to(dev)
+        sv = inputs.signs(a.cols, 2).to(dev)
+        out = torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev)
+        ws = torch.empty(ex.regularize_workspace_bytes(a.rows, a.cols), dtype=torch.uint8, device=dev)
+        fn = lambda: ex.regularize(W, h, sv, W_out=out, ws=ws)
+    elif a.case in ("ldl", "ldlq"):
+        H = inputs.spd_hessian(a.rows, 0, rho=0.95).to(dev)
+        M = torch.empty(a.rows, a.rows, dtype=torch.float32, device=dev)
+        wl = torch.empty(ex.block_ldl_workspace_bytes(a.rows), dtype=torch.uint8, device=dev)
+        ex.block_ldl(H, M=M, ws=wl)
+        if a.case == "ldl":
+            fn = lambda: ex.block_ldl(H, M=M, ws=wl)
+        else:
+            del wl
+            R = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+            wq = torch.empty(ex.ldlq_workspace_bytes(a.rows, a.cols, a.K), dtype=torch.uint8,
+                             device=dev)
+            codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
+            fn = lambda: ex.ldlq(R, M, a.K, 1.0, want_q=False, codes=codes, ws=wq)
     else:
         W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
         su, sv = (t.to(dev) for t in inputs.sign_pair(a.rows, a.cols, 0))

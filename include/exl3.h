@@ -313,6 +313,43 @@ EXL3_API exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const
                                void *stream);
 
 /*
+ * Output-channel regularisation of a weight before rotation (README item 8:
+ * block_rms with a 32-slice accumulation order, the output-scale skew
+ * heuristic on the top 2 % of sqrt(H_diag) against a 15 % cutoff, output-channel
+ * RMS normalisation with sign and scale folded into sv, and the zero-channel
+ * floor 0.1 with sv = 0).  The README names the parts only; this library reads
+ * them as follows.
+ *   S_c      : the rows cut into 32 consecutive slices of ceil(rows / 32) rows;
+ *              each slice's binary64 sum of w^2 in row order; the slice sums
+ *              added in slice order (block_rms of channel c = sqrt(S_c / rows));
+ *   skew     : d = sqrt(h) (binary64) sorted descending; skew = tree(the first
+ *              max(1, rows / 50)) / tree(all), binary64 pairwise trees over the
+ *              sorted values (neighbours (2i, 2i+1) per level, an odd last
+ *              element moves up), 0 when the total is 0;
+ *   scale_c  : 0.1 when S_c = 0 (sv_out[c] = 0: the channel decodes to zero);
+ *              otherwise fl32(sqrt(S_c / rows)) when the output scales apply,
+ *              else the global fl32(sqrt(T / (rows * cols))), T = the S_c added
+ *              as a pairwise tree; the output scales apply when skew < 0.15
+ *              (apply_out = -1) or when forced (apply_out = 1; 0 forces off);
+ *   W_out    : fl32(W[r][c] / scale_c); sv_out[c] = sv[c] * scale_c.
+ * The inverse rotation with sv_out in place of the signs sv undoes the
+ * normalisation (the decode multiplies by sv as given).
+ *   W bf16/fp32 [rows, cols]: input channels down the rows, output channels
+ *     across; rows in [1, 65536], cols in [1, 2^24].  W_out (device) float
+ *     [rows, cols] may equal W when W is fp32.
+ *   h (device) float [rows]: the Hessian's diagonal, >= 0; sv (device) float
+ *     [cols]: output-channel signs.
+ *   sv_out (device) float [cols] out; info_out (device) double [4] or NULL:
+ *     {skew, output scales applied (0/1), all-zero weight (0/1), global RMS}.
+ *   ws: exl3_regularize_workspace_bytes(rows, cols).
+ */
+EXL3_API size_t exl3_regularize_workspace_bytes(int64_t rows, int64_t cols);
+EXL3_API exl3_status exl3_regularize(const void *W, int dt, int64_t rows, int64_t cols,
+                                     const float *h, const float *sv, int apply_out,
+                                     float *W_out, float *sv_out, double *info_out, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/*
  * exl3_encode_tiles without a workspace, for callers that cannot allocate
  * device memory (no counterpart on the pages: an interface addition of this
  * library).  Such callers include plug-ins running inside an application that

@@ -84,6 +84,7 @@ def _load():
         L.ora_cholesky_damped.restype = i32
         L.ora_block_fold.argtypes = [P, i64, P]
         L.ora_ldlq_feedback.argtypes = [P, P, i64, i64, i64, P]
+        L.ora_block_sumsq_cols.argtypes = [P, i64, i64, i32, P]
         _lib = L
         return L
 

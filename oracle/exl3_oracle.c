@@ -34,6 +34,9 @@
  *           2 * sigma_reg * mean(diag H) up to 10 times, bottom-up error
  *           feedback from the strictly lower part of M into the targets of the
  *           rows not yet quantised.
+ *   [Reg]   item 8, "Weight Regularization & Global-Scale Search": block_rms
+ *           accumulated over 32 slices, output-channel RMS normalisation
+ *           folded into sv.
  *
  * Readings fixed where the pages are silent (each also listed in the design
  * notes of the repository):
@@ -577,5 +580,34 @@ void ora_ldlq_feedback(float *acc, const float *M, int64_t n, int64_t cols, int6
                 a = fmaf(M[i * n + r], E[(i - 16 * j) * cols + c], a);
             acc[r * cols + c] = a;
         }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Output-channel regularisation  [Reg]                                      */
+/* ------------------------------------------------------------------------ */
+
+/* block_rms accumulation of every column of W [rows, cols] (fp32): the rows
+ * are cut into `slices` consecutive slices of ceil(rows / slices) rows (the
+ * last may be shorter or empty); each slice's sum of squares is accumulated
+ * in binary64 in ascending row order starting from 0, and the slice sums are
+ * added in slice order.  out[c] = that total (the caller takes
+ * sqrt(out[c] / rows)). */
+void ora_block_sumsq_cols(const float *W, int64_t rows, int64_t cols, int slices, double *out)
+{
+    const int64_t len = (rows + slices - 1) / slices;
+    for (int64_t c = 0; c < cols; c++) {
+        double total = 0.0;
+        for (int s = 0; s < slices; s++) {
+            double part = 0.0;
+            const int64_t r0 = (int64_t)s * len;
+            const int64_t r1 = r0 + len < rows ? r0 + len : rows;
+            for (int64_t r = r0; r < r1; r++) {
+                const double w = (double)W[r * cols + c];
+                part = part + w * w;
+            }
+            total = total + part;
+        }
+        out[c] = total;
     }
 }

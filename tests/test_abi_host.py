@@ -148,6 +148,21 @@ def test_ldl_and_ldlq_reject_bad_arguments(ex):
     assert lq(K=1, w=fixed + ex.encode_workspace_min_bytes(2)) == 3
 
 
+def test_regularize_rejects_bad_arguments(ex):
+    L = ex.lib()
+    w = ex.regularize_workspace_bytes(64, 32)
+    rg = lambda rows=64, cols=32, dt=1, W=FAKE, Wo=ctypes.c_void_p(0x20000000), ap=-1, ws=w: \
+        L.exl3_regularize(W, dt, rows, cols, FAKE, FAKE, ap, Wo, FAKE, None, FAKE, ws, None)
+    assert rg(rows=0) == 2 and rg(cols=0) == 2 and rg(rows=65537) == 2
+    assert rg(dt=7) == 1
+    assert rg(W=None) == 1
+    assert rg(ap=2) == 1 and rg(ap=-2) == 1
+    assert rg(Wo=FAKE) == 1                     # in place needs an fp32 W
+    assert rg(dt=0, Wo=FAKE, ws=100) == 3       # fp32 in place is fine; workspace too small
+    assert ex.regularize_workspace_bytes(64, 32) > 32 * 32 * 8
+    assert ex.regularize_workspace_bytes(0, 32) == 0
+
+
 def test_workspace_queries_scale_with_work(ex):
     a = ex.encode_workspace_bytes(10, 2)
     b = ex.encode_workspace_bytes(100000, 2)

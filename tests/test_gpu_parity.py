@@ -530,3 +530,99 @@ def test_ldlq_full_size_properties(ex):
     l1 = ((H @ E1) * E1).sum().item()
     l0 = ((H @ E0) * E0).sum().item()
     assert l1 < 0.8 * l0
+
+
+# ---------------------------------------------------------------------------
+# output-channel regularisation
+# ---------------------------------------------------------------------------
+
+def _reg_case(rows, cols, seed, kind):
+    g = np.random.default_rng(seed)
+    W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02, outlier_frac=0.001)
+    W = (W.float() * torch.from_numpy(g.uniform(0.05, 4.0, cols).astype(np.float32))).to(torch.bfloat16)
+    h = inputs.hessian_diag(rows, seed).numpy().copy()
+    if kind == "spiky":
+        h[::40] *= 1e4
+    sv = inputs.signs(cols, seed + 2)
+    return W, torch.from_numpy(h), sv
+
+
+@pytest.mark.parametrize("rows,cols,seed,kind,apply_out", [
+    (256, 384, 61, "flat", -1), (256, 384, 62, "spiky", -1), (128, 64, 63, "flat", 0),
+    (512, 16, 64, "spiky", 1), (100, 33, 65, "flat", -1), (7, 5, 66, "flat", -1),
+    (20000, 16, 67, "spiky", -1)])      # 20000 rows: the sort runs in global memory
+def test_regularize_matches_oracle(ex, rows, cols, seed, kind, apply_out):
+    from oracle import regularize as OR
+    W, h, sv = _reg_case(rows, cols, seed, kind)
+    W[:, 3 % cols] = 0
+    r = ex.regularize(W.to(DEV), h.to(DEV), sv.to(DEV), apply_out=apply_out)
+    torch.cuda.synchronize()
+    ref = OR.regularize(W.float().numpy(), h.numpy(), sv.numpy(), apply_out=apply_out)
+    info = r["info"].cpu().numpy()
+    assert info[0] == ref["skew"]
+    assert bool(info[1]) == ref["apply_out"] and not info[2]
+    assert info[3] == ref["rms"]
+    if apply_out < 0 and rows >= 100:      # with 7 rows the top 2 % is one channel
+        assert ref["apply_out"] == (kind == "flat")
+    assert np.array_equal(r["sv_out"].cpu().numpy(), ref["sv_out"])
+    assert np.array_equal(r["W_out"].cpu().numpy(), ref["W_out"])
+
+
+def test_regularize_extreme_bf16_magnitudes(ex):
+    """bf16 values whose squares leave fp32's normal range (tiny, subnormal and
+    huge) take the binary64 square: S_c still matches the oracle exactly."""
+    from oracle import regularize as OR
+    vals = torch.tensor([1e-30, 3e-39, 1e-20, 0.5, 3e25, -2e30, 7.0, 0.0], dtype=torch.float32)
+    W = vals.repeat(64, 4).reshape(64, 32).to(torch.bfloat16)
+    h = torch.ones(64)
+    sv = torch.ones(32)
+    r = ex.regularize(W.to(DEV), h.to(DEV), sv.to(DEV), apply_out=1)
+    torch.cuda.synchronize()
+    ref = OR.regularize(W.float().numpy(), h.numpy(), sv.numpy(), apply_out=1)
+    assert np.array_equal(r["sv_out"].cpu().numpy(), ref["sv_out"])
+    assert np.array_equal(r["W_out"].cpu().numpy(), ref["W_out"])
+
+
+def test_regularize_all_zero_and_in_place(ex):
+    from oracle import regularize as OR
+    Z = torch.zeros(64, 48, device=DEV)
+    r = ex.regularize(Z, torch.ones(64, device=DEV), torch.ones(48, device=DEV))
+    info = r["info"].cpu().numpy()
+    assert info[2] == 1.0 and not r["sv_out"].any().item() and not r["W_out"].any().item()
+    W, h, sv = _reg_case(256, 128, 70, "flat")
+    Wf = W.float().to(DEV)
+    r = ex.regularize(Wf, h.to(DEV), sv.to(DEV), W_out=Wf)
+    torch.cuda.synchronize()
+    ref = OR.regularize(W.float().numpy(), h.numpy(), sv.numpy())
+    assert np.array_equal(Wf.cpu().numpy(), ref["W_out"])
+
+
+def test_regularize_full_size_and_round_trip(ex):
+    """12288 x 4096 bf16 (a 12288-input projection) against the oracle, then the
+    chain regularise -> quantize -> decode -> inverse rotation with sv_out."""
+    from oracle import regularize as OR
+    W, h, sv = _reg_case(12288, 4096, 71, "flat")
+    r = ex.regularize(W.to(DEV), h.to(DEV), sv.to(DEV))
+    torch.cuda.synchronize()
+    ref = OR.regularize(W.float().numpy(), h.numpy(), sv.numpy())
+    assert np.array_equal(r["sv_out"].cpu().numpy(), ref["sv_out"])
+    assert np.array_equal(r["W_out"].cpu().numpy(), ref["W_out"])
+    # round trip on a smaller slab, compared with the oracle's chain
+    Ws, hs, svs = _reg_case(256, 512, 72, "flat")
+    su = inputs.signs(256, 73)
+    r = ex.regularize(Ws.to(DEV), hs.to(DEV), svs.to(DEV))
+    q = ex.quantize(r["W_out"], su.to(DEV), svs.to(DEV), 3, 1.0)
+    s = float(q["scale"].item())
+    Qd = ex.decode_tiles(q["codes"], 256, 512, 3, s)
+    What = ex.rotate(Qd, su.to(DEV), r["sv_out"], inverse=True)
+    torch.cuda.synchronize()
+    ref = OR.regularize(Ws.float().numpy(), hs.numpy(), svs.numpy())
+    Rn = oracle.rotate_forward(ref["W_out"], su.numpy(), svs.numpy())
+    assert s == oracle.scale_for(1.0, oracle.rms(Rn))[0]
+    codes_o = oracle.codes_from_states(oracle.encode_matrix(Rn, 3, 1.0 / np.float32(s))[0], 256, 512, 3)
+    Qo = oracle.decode_matrix(codes_o, 256, 512, 3, s)
+    What_o = oracle.rotate_inverse(Qo, su.numpy(), ref["sv_out"])
+    assert np.array_equal(What.cpu().numpy(), What_o)
+    Wd = Ws.float().numpy().astype(np.float64)
+    rel = np.sum((What_o - Wd) ** 2) / np.sum(Wd ** 2)
+    assert rel < 0.05          # K=3 keeps the relative error near 2^-6
