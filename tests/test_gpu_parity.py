@@ -422,11 +422,13 @@ def test_scale_search_full_size_properties(ex):
         assert g == h[26, 0]
     else:
         assert g == fine[np.argmin(fine[:, 1]), 0]
-    # recompute the full-sample MSE at the chosen g with the oracle
+    # the oracle's whole search on the same matrix: every (g, MSE) point exact
     R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
-    S = ss.sample_tiles(oracle.tile_sumsq(R), 256, 256)
-    f = ss.subset_mse(R, S, K, g, oracle.rms(R))
-    assert f == min(fine[:, 1].min(), h[26, 1] if h[26, 0] >= 0 else np.inf)
+    ref = ss.grid_scale_search(R, K)
+    want = np.array(ref["coarse"] + ref["fine"] +
+                    [ref["refined"] if ref["refined"] is not None else (-1.0, -1.0)])
+    assert np.array_equal(h, want)
+    assert g == ref["g"]
 
 
 # ---------------------------------------------------------------------------
@@ -501,14 +503,20 @@ def test_ldlq_small_workspace_and_no_q(ex):
 
 
 def test_ldlq_full_size_properties(ex):
-    """4096 x 4096 K=2 with a 4096-channel synthetic Hessian: the factor
-    block-diagonalises H, the bottom span is plain quantisation (oracle), and
-    the feedback lowers the Hessian-weighted error against plain coding."""
+    """4096 x 4096 K=2 with a 4096-channel synthetic Hessian: the factor is
+    bit-exact against the oracle's (all 16.8 M entries) and block-diagonalises
+    H; the two bottom spans (which read nothing above them) match the oracle's
+    LDLQ of R's bottom 32 rows with M's bottom-right 32 x 32 block; the feedback
+    lowers the Hessian-weighted error against plain coding."""
     from oracle import ldlq as OL
     n, cols, K = 4096, 4096, 2
-    H = inputs.spd_hessian(n, 50, rho=0.95).to(DEV)
+    Hc = inputs.spd_hessian(n, 50, rho=0.95)
+    H = Hc.to(DEV)
     M, a = ex.block_ldl(H)
     assert a == 0
+    Mo, ao, _ = OL.block_ldl(Hc.numpy())
+    assert ao == 0
+    assert np.array_equal(M.cpu().numpy(), Mo)
     U = M.double() + torch.eye(n, dtype=torch.float64, device=DEV)
     Y = torch.linalg.solve_triangular(U, H, upper=False)
     Z = torch.linalg.solve_triangular(U, Y.T.contiguous(), upper=False)   # U^-1 H U^-T
@@ -524,6 +532,9 @@ def test_ldlq_full_size_properties(ex):
     bottom = res["codes"][-1:].cpu().numpy().view(np.uint16).reshape(-1, 16 * K)
     want, _ = _oracle_codes(R.numpy()[n - 16:], K, float(np.float32(1.0) / np.float32(s)))
     assert np.array_equal(bottom, want)
+    ref = OL.ldlq(R.numpy()[n - 32:], Mo[n - 32:, n - 32:], K, s)
+    assert np.array_equal(res["codes"][-2:].cpu().numpy().view(np.uint16), ref["codes"])
+    assert np.array_equal(res["Q"][n - 32:].cpu().numpy(), ref["Q"])
     plain = ex.ldlq(Rd, torch.zeros_like(M), K, s)
     E1 = (Rd - res["Q"]).double()
     E0 = (Rd - plain["Q"]).double()
