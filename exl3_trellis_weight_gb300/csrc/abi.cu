@@ -178,9 +178,16 @@ __global__ void scale_kernel(const double *sum, int64_t n, double g, const doubl
     if (sigma == 0.0)
         sigma = 1.0;   // all-zero matrix: any scale codes it; use g itself
     const double gg = g_dev ? *g_dev : g;
-    const float s = __double2float_rn(__dmul_rn(gg, sigma));
+    float s = __double2float_rn(__dmul_rn(gg, sigma));
+    float inv = __fdiv_rn(1.0f, s);
+    if (!isfinite(sigma) || !isfinite(s) || !isfinite(inv)) {
+        // a non-finite weight (or a scale out of binary32 range) is rejected:
+        // NaN scale, and the encode kernels skip every tile when 1/s is not finite
+        s = __int_as_float(0x7fffffff);
+        inv = s;
+    }
     fscal[0] = s;
-    fscal[1] = __fdiv_rn(1.0f, s);
+    fscal[1] = inv;
     if (sigma_out) *sigma_out = sigma;
     if (scale_out) *scale_out = s;
 }
@@ -445,8 +452,8 @@ exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K,
     if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
     if (tile_cost && !aligned(tile_cost, 4))
         return set_error(EXL3_ERR_INVALID_ARG, "tile_cost is not 4-byte aligned");
-    if (!(scale > 0.0f) || !std::isfinite(scale))
-        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (!(scale > 0.0f) || !std::isfinite(scale) || !std::isfinite(1.0f / scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale and 1 / scale must be positive and finite");
     if (!ws || !aligned(ws, kAlign))
         return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
     const int64_t n_tiles = (rows / 16) * (cols / 16);
@@ -491,8 +498,8 @@ exl3_status exl3_encode_rows(const float *Y, int64_t n_rows, int T, int K, float
     if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
     if (row_cost && !aligned(row_cost, 4))
         return set_error(EXL3_ERR_INVALID_ARG, "row_cost is not 4-byte aligned");
-    if (!(scale > 0.0f) || !std::isfinite(scale))
-        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (!(scale > 0.0f) || !std::isfinite(scale) || !std::isfinite(1.0f / scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale and 1 / scale must be positive and finite");
     if (!ws || !aligned(ws, kAlign))
         return set_error(EXL3_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
     const int64_t grid = fit_blocks(encode_grid_full(n_rows, K),
@@ -823,8 +830,8 @@ exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M
         return set_error(EXL3_ERR_UNSUPPORTED, "rows and cols must be positive multiples of 16");
     if ((st = check_ptr(M, "M", 4)) != EXL3_OK) return st;
     if ((st = check_k(K)) != EXL3_OK) return st;
-    if (!(scale > 0.0f) || !std::isfinite(scale))
-        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (!(scale > 0.0f) || !std::isfinite(scale) || !std::isfinite(1.0f / scale))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale and 1 / scale must be positive and finite");
     if ((st = check_ptr(codes, "codes", 4)) != EXL3_OK) return st;
     if (Q && !aligned(Q, 4))
         return set_error(EXL3_ERR_INVALID_ARG, "Q is not 4-byte aligned");

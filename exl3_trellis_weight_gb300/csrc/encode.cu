@@ -164,7 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     const int tiles_c = row_tiles ? 1 : (int)(a.cols / 16);
     const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
     const int grid = (int)gridDim.x;
-    const int n_my = n_tiles > (int)blockIdx.x ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
+    // a non-finite inverse scale (a rejected weight, see scale_kernel) codes no tile
+    const int n_my = (isfinite(inv_s) && n_tiles > (int)blockIdx.x)
+                         ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
     // decision buffers of this block: pass-1 slots 0/1, then pass-2 slots 0/1
     uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
     constexpr size_t kP1 = (size_t)kRowsPass1 * kRowWords, kP2 = (size_t)kRowsPass2 * kRowWords;

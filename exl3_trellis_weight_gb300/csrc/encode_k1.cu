@@ -178,7 +178,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
     const int cid = (int)blockIdx.x >> 1;
     const int n_clusters = (int)gridDim.x >> 1;
-    const int n_my = n_tiles > cid ? (n_tiles - cid + n_clusters - 1) / n_clusters : 0;
+    // a non-finite inverse scale (a rejected weight) codes no tile; both blocks
+    // of a cluster read the same scalar, so they skip the same barriers
+    const int n_my = (isfinite(inv_s) && n_tiles > cid)
+                         ? (n_tiles - cid + n_clusters - 1) / n_clusters : 0;
     uint32_t *const scr = a.scratch + (size_t)blockIdx.x * kBlockWords;       // own slice
     uint32_t *const scr0 = a.scratch + (size_t)(2 * cid) * kBlockWords;       // block 0's slice
     constexpr size_t kP1 = (size_t)kRowsPass1 * kRowWords, kP2 = (size_t)kRowsPass2 * kRowWords;

@@ -75,8 +75,8 @@ extern "C" EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_
                          (long long)cols);
     if (K < 2 || K > 4)
         return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: the workspace-free encode takes K in {2,3,4}", K);
-    if (!(scale > 0.0f) || !(scale < __builtin_inff()))
-        return set_error(EXL3_ERR_INVALID_ARG, "scale must be positive and finite");
+    if (!(scale > 0.0f) || !(scale < __builtin_inff()) || !(1.0f / scale < __builtin_inff()))
+        return set_error(EXL3_ERR_INVALID_ARG, "scale and 1 / scale must be positive and finite");
     if (blocks < 0 || blocks > kNoAllocMaxBlocks)
         return set_error(EXL3_ERR_WORKSPACE,
                          "blocks=%d exceeds the static scratch: at most %d blocks (%zu bytes each)",

@@ -29,9 +29,11 @@
  *     status nothing was enqueued (except EXL3_ERR_CUDA, which reports a
  *     failed launch) and no output is promised.  exl3_last_error() returns a
  *     message for the calling thread's last failure.
- *   - Inputs must be finite.  Non-finite inputs produce unspecified codes and
- *     values but never an out-of-bounds access: every data-dependent index in
- *     the kernels is masked to its table.
+ *   - Inputs must be finite.  exl3_quantize and exl3_gss_scale detect a
+ *     non-finite weight on the device and code nothing (see exl3_quantize);
+ *     elsewhere non-finite inputs produce unspecified codes and values but
+ *     never an out-of-bounds access: every data-dependent index in the kernels
+ *     is masked to its table.
  *   - Arithmetic: IEEE binary32 with round-to-nearest and no FMA contraction
  *     on the encode/decode/rotation path; binary64 for reductions and the
  *     search.  Results are bit-for-bit reproducible run to run.
@@ -187,6 +189,11 @@ EXL3_API exl3_status exl3_mse(const void *W, int dt, const float *What, int64_t 
  *   mse_out (device) double.   sigma_out (device) double or NULL.
  *   What (device) fp32 [rows, cols] or NULL to skip writing it.
  *   ws: exl3_quantize_workspace_bytes(rows, cols, K) for the full machine.
+ * A non-finite weight is rejected on the device (the call does not
+ * synchronise, so the status stays EXL3_OK): when sigma, s or 1/s is not
+ * finite, scale_out is NaN, no tile is coded (codes keep their previous
+ * contents), and mse_out and What are NaN; sigma_out shows the cause.
+ * exl3_gss_scale inherits this for every evaluation.
  */
 EXL3_API size_t exl3_quantize_workspace_bytes(int64_t rows, int64_t cols, int K);
 EXL3_API exl3_status exl3_quantize(const void *W, int dt, int64_t rows, int64_t cols,

@@ -76,6 +76,7 @@ def test_encode_rejects_bad_arguments(ex):
     assert call(scale=ctypes.c_float(0.0)) == 1
     assert call(scale=ctypes.c_float(float("inf"))) == 1
     assert call(scale=ctypes.c_float(float("nan"))) == 1
+    assert call(scale=ctypes.c_float(1e-45)) == 1          # 1 / scale overflows to inf
     assert call(ws_bytes=ws_min - 1) == 3                   # workspace too small
     assert call(ws=None) == 1
     assert call(ws=ctypes.c_void_p(0x10000010)) == 1        # workspace not 256-aligned

@@ -637,3 +637,31 @@ def test_regularize_full_size_and_round_trip(ex):
     Wd = Ws.float().numpy().astype(np.float64)
     rel = np.sum((What_o - Wd) ** 2) / np.sum(Wd ** 2)
     assert rel < 0.05          # K=3 keeps the relative error near 2^-6
+
+
+# ---------------------------------------------------------------------------
+# non-finite weights are rejected on the device
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", [1, 2])
+def test_quantize_rejects_non_finite_weight(ex, K):
+    import math
+    W = inputs.linear_bf16(256, 256, seed=80)
+    su, sv = (t.to(DEV) for t in inputs.sign_pair(256, 256, 80))
+    for bad in (float("nan"), float("inf")):
+        Wb = W.clone()
+        Wb[17, 33] = bad
+        codes = torch.full((16, 16, 16 * K), 0x1234, dtype=torch.int16, device=DEV)
+        r = ex.quantize(Wb.to(DEV), su, sv, K, 1.0, codes=codes)
+        torch.cuda.synchronize()
+        assert math.isnan(r["scale"].item()) and math.isnan(r["mse"].item())
+        assert not math.isfinite(r["sigma"].item())
+        assert bool((codes == 0x1234).all().item())          # no tile was coded
+    # the context stays usable: a clean call matches the oracle
+    r = ex.quantize(W.to(DEV), su, sv, K, 1.0)
+    torch.cuda.synchronize()
+    R = oracle.rotate_forward(W.float().numpy(), su.cpu().numpy(), sv.cpu().numpy())
+    s, inv = oracle.scale_for(1.0, oracle.rms(R))
+    assert float(r["scale"].item()) == s
+    want, _ = _oracle_codes(R, K, inv)
+    assert np.array_equal(_np_codes(r["codes"], K), want)
