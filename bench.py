@@ -50,7 +50,7 @@ ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
     # `ncu --set full` on 1,216 tiles (profiles/encode_k2_small.md); the traffic is
     # the decision rows, proportional to the tiles processed.
-    "49cc31fcb344f9cf2c3183bfd2e28d6066f32281c8c1a8e76ca1cd20b5b1605e": 1545517.0,
+    "36bba21314bc4c80f2b5ddd9e4436322fd4c311bbc344bac8df95c1dbc57f75d": 1545546.0,
 }
 
 WORKLOAD = "linear4096_k2"
@@ -436,7 +436,30 @@ def run_ours(args):
                        "spans": rows // 16, "tiles_per_span": cols // 16,
                        "encode_share": (lq_enc_ms / len(lq_ms)) / lq_avg,
                        "encode_launches": lq_enc_n // len(lq_ms)}
-        del ws_q, codes_q, R, M, Hd
+        del ws_q, codes_q, R
+        # q | k | v of one attention layer (4096 + 1024 + 1024 output channels) share
+        # the input Hessian: one LDLQ call on the column concatenation codes 384
+        # tiles per span instead of 256 + 64 + 64 in three calls
+        qkv_cols = cols + 2 * (cols // 4)
+        Rq = inputs.iid_f32(rows, qkv_cols, 53).to(dev)
+        ws_q = torch.empty(ex.ldlq_workspace_bytes(rows, qkv_cols, K), dtype=torch.uint8, device=dev)
+        codes_q = torch.empty(rows // 16, qkv_cols // 16, 16 * K, dtype=torch.int16, device=dev)
+        ex.ldlq(Rq, M, K, 1.0, want_q=False, codes=codes_q, ws=ws_q)
+        torch.cuda.synchronize(dev)
+        qkv_ms = []
+        for _ in range(2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.ldlq(Rq, M, K, 1.0, want_q=False, codes=codes_q, ws=ws_q)
+            b.record(stream)
+            b.synchronize()
+            qkv_ms.append(a.elapsed_time(b))
+        qkv_avg = sum(qkv_ms) / len(qkv_ms)
+        aux["ldlq_qkv"] = {"ms": qkv_avg, "cols": qkv_cols,
+                           "tiles_per_s": (rows // 16) * (qkv_cols // 16) / (qkv_avg / 1e3),
+                           "what": "q|k|v column concatenation, one call, N(0,1) targets, scale 1"}
+        del ws_q, codes_q, Rq, M, Hd
 
         # output-channel regularisation of the same weight (synthetic Hessian diagonal)
         h_d = inputs.hessian_diag(rows, 52).to(dev)
