@@ -175,6 +175,10 @@ struct RotateLaunch {
     double *tile_sums;        // per-tile sums: of out^2 (ref == null) or of (ref-out)^2
 };
 exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s);
+// forward path without lane exchanges (rotate_fwd.cu): fp32/bf16 source, no ref,
+// 16-byte aligned in / sv / out; launch_rotate picks it when eligible
+bool rotate_fwd_eligible(const RotateLaunch &p);
+exl3_status launch_rotate_fwd(const RotateLaunch &p, cudaStream_t s);
 
 // grid-and-parabola scale search (scale_search.cu)
 struct GridSearchLaunch {

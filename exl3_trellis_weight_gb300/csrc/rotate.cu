@@ -292,6 +292,8 @@ exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s) {
     const int64_t nblk = (p.rows / 128) * (p.cols / 128);
     if (nblk == 0)
         return EXL3_OK;
+    if (rotate_fwd_eligible(p))
+        return launch_rotate_fwd(p, s);
     const size_t smem = (size_t)128 * kPitch * sizeof(float) + (size_t)64 * 32 * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(rotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

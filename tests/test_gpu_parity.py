@@ -170,6 +170,30 @@ def test_rotate_in_place_fp32(ex):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_rotate_forward_unaligned_views(ex, dt):
+    """Inputs and outputs that are not 16-byte aligned take the shuffle-based
+    kernel; aligned ones the shared-memory one: both give the oracle's bits,
+    including non-unit sign vectors (su, sv multiplied as given)."""
+    rows, cols = 128, 384
+    W = inputs.linear_bf16(rows, cols, seed=11, std=0.02)
+    if dt == "f32":
+        W = W.float()
+    su = inputs.signs(rows, 12) * 0.75
+    sv = inputs.signs(cols, 13) * 1.25
+    want = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    n = rows * cols
+    buf = torch.empty(n + 8, dtype=W.dtype, device=DEV)
+    Wu = buf[1:1 + n].view(rows, cols)                  # element offset 1: 2 or 4 bytes
+    Wu.copy_(W.to(DEV))
+    obuf = torch.empty(n + 8, dtype=torch.float32, device=DEV)
+    out_u = obuf[2:2 + n].view(rows, cols)              # 8-byte offset
+    for src, out in ((W.to(DEV), None), (Wu, None), (W.to(DEV), out_u), (Wu, out_u)):
+        R = ex.rotate(src, su.to(DEV), sv.to(DEV), out=out)
+        torch.cuda.synchronize()
+        assert np.array_equal(R.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_mse_fixed_order(ex, dt):
     rows, cols = 256, 512
     W = inputs.linear_bf16(rows, cols, seed=11)
