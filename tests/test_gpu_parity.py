@@ -301,6 +301,15 @@ def _check_full(ex, W, su, sv, K, n_sample, seed):
     want, _ = _oracle_codes(R, K, inv, tiles=idx)
     got = _np_codes(res["codes"], K)[idx]
     assert np.array_equal(got, want)
+    # the decoded weights of the sampled tiles (rotated domain, fl(v * s))
+    Yhat = ex.decode_tiles(res["codes"], rows, cols, K, s)
+    torch.cuda.synchronize()
+    Yh = Yhat.cpu().numpy()
+    tc = cols // 16
+    for t, words in zip(idx, want):
+        vals = oracle.decode_values(oracle.unpack_states(words, K), s).reshape(16, 16)
+        r0, c0 = (t // tc) * 16, (t % tc) * 16
+        assert np.array_equal(Yh[r0:r0 + 16, c0:c0 + 16], vals)
     return res
 
 
@@ -322,7 +331,7 @@ def test_full_linear4096_k1_sampled(ex):
     _check_full(ex, W, su, sv, 1, 24, 5)
 
 
-@pytest.mark.parametrize("proj", ["k", "down"])
+@pytest.mark.parametrize("proj", ["q", "k", "v", "o", "gate", "up", "down"])
 def test_full_layer_k3_sampled(ex, proj):
     for lab, W, su, sv, K in inputs.workload("layer4096_k3"):
         if lab == proj:
