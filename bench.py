@@ -45,7 +45,7 @@ ALU_LANES_PER_SM_CLK = 128
 SM_MAX_MHZ_NOMINAL = 2070.0
 
 # DRAM traffic of one encode launch per tile, from an ncu capture
-# (profiles/encode_k2_linear4096.md); valid only for the source it was taken on.
+# (profiles/encode_k2_small.md); valid only for the source it was taken on.
 ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
     # `ncu --set full` on 1,216 tiles (profiles/encode_k2_small.md); the traffic is
@@ -482,6 +482,54 @@ def run_ours(args):
                              "bytes": rg_bytes, "applied": bool(rr["info"][1].item()),
                              "skew": float(rr["info"][0].item())}
         del W_o, ws_r, h_d
+
+        # the 12-evaluation golden-section search on 4096x4096 K=2 (12 quantize passes)
+        (_, Wg, sug, svg, Kg), = inputs.workload("gss4096_k2")
+        Wg, sug, svg = Wg.to(dev), sug.to(dev), svg.to(dev)
+        ws_g = torch.empty(ex.gss_workspace_bytes(rows, cols, Kg), dtype=torch.uint8, device=dev)
+        ex.gss_scale(Wg, sug, svg, Kg, 0.5, 2.0, 12, ws=ws_g)
+        torch.cuda.synchronize(dev)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rg = ex.gss_scale(Wg, sug, svg, Kg, 0.5, 2.0, 12, ws=ws_g)
+        b.record(stream)
+        b.synchronize()
+        gss_ms = a.elapsed_time(b)
+        aux["gss12"] = {"ms": gss_ms, "tiles_per_s": 12 * n_tiles / (gss_ms / 1e3),
+                        "g": float(rg["g"].item()), "mse": float(rg["mse"].item()),
+                        "workload": "gss4096_k2: 4096x4096 bf16 N(0, 0.02^2), K=2, [0.5, 2.0]"}
+        del ws_g, Wg, sug, svg
+
+        # all seven projections of one decoder layer at K=3 (753,664 tiles), one pass
+        layer = [(lab, Wl, sul, svl) for lab, Wl, sul, svl, _ in inputs.workload("layer4096_k3")]
+        ws_l = torch.empty(max(ex.quantize_workspace_bytes(*Wl.shape, 3) for _, Wl, _, _ in layer),
+                           dtype=torch.uint8, device=dev)
+        ex.quantize(layer[1][1].to(dev), layer[1][2].to(dev), layer[1][3].to(dev), 3, 1.0, ws=ws_l)
+        torch.cuda.synchronize(dev)
+        lay_ms, lay_tiles = 0.0, 0
+        ex.profile_enable(True)
+        for lab, Wl, sul, svl in layer:
+            Wd, sud, svd = Wl.to(dev), sul.to(dev), svl.to(dev)
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.quantize(Wd, sud, svd, 3, 1.0, ws=ws_l)
+            b.record(stream)
+            b.synchronize()
+            lay_ms += a.elapsed_time(b)
+            lay_tiles += (Wl.shape[0] // 16) * (Wl.shape[1] // 16)
+            del Wd, sud, svd
+        l_enc_ms, l_enc_n, _ = ex.profile_read()
+        ex.profile_enable(False)
+        ach3 = alg_ops_per_tile(3) * lay_tiles / (l_enc_ms / 1e3) / 1e12
+        aux["layer_k3"] = {"ms": lay_ms, "tiles": lay_tiles,
+                           "tiles_per_s": lay_tiles / (lay_ms / 1e3),
+                           "encode_tiles_per_s": lay_tiles / (l_enc_ms / 1e3),
+                           "roofline_frac": ach3 / peak_tops,
+                           "workload": "layer4096_k3: q, k, v, o, gate, up, down of a 4096-hidden, "
+                                       "12288-intermediate, 8-KV-head layer, bf16 N(0, 0.02^2), K=3"}
+        del ws_l, layer
 
     # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
     cpu = None
