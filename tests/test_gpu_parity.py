@@ -698,3 +698,34 @@ def test_quantize_rejects_non_finite_weight(ex, K):
     assert float(r["scale"].item()) == s
     want, _ = _oracle_codes(R, K, inv)
     assert np.array_equal(_np_codes(r["codes"], K), want)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graph capture: the quantize chain and the GSS enqueue no host syncs
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", [1, 2])
+def test_quantize_and_gss_replay_from_cuda_graph(ex, K):
+    rows, cols = 256, 256
+    W = inputs.linear_bf16(rows, cols, seed=90)
+    su, sv = (t.to(DEV) for t in inputs.sign_pair(rows, cols, 90))
+    Wd = W.to(DEV)
+    ws = torch.empty(ex.gss_workspace_bytes(rows, cols, K), dtype=torch.uint8, device=DEV)
+    direct = ex.quantize(Wd, su, sv, K, 1.3, ws=ws)
+    gdirect = ex.gss_scale(Wd, su, sv, K, 0.5, 2.0, 6, ws=ws)
+    torch.cuda.synchronize()
+    codes = torch.zeros_like(direct["codes"])
+    gcodes = torch.zeros_like(gdirect["codes"])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        q = ex.quantize(Wd, su, sv, K, 1.3, codes=codes, ws=ws)
+        gs = ex.gss_scale(Wd, su, sv, K, 0.5, 2.0, 6, best_codes=gcodes, ws=ws)
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(codes, direct["codes"])
+        assert float(q["mse"].item()) == float(direct["mse"].item())
+        assert torch.equal(gcodes, gdirect["codes"])
+        assert float(gs["g"].item()) == float(gdirect["g"].item())
+        codes.zero_()
+        gcodes.zero_()
