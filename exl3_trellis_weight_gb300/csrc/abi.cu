@@ -817,7 +817,8 @@ static size_t ldlq_carve(void *ws, int64_t rows, int64_t cols, int grid, LdlqLau
 }
 
 size_t exl3_ldlq_workspace_bytes(int64_t rows, int64_t cols, int K) {
-    if (!k_ok(K) || rows < 16 || cols < 16 || rows % 16 || cols % 16)
+    if (!k_ok(K) || rows < 16 || cols < 16 || rows % 16 || cols % 16 || rows > (1ll << 24) ||
+        cols > (1ll << 24) || rows * cols > (1ll << 34))
         return 0;
     return ldlq_carve(nullptr, rows, cols, encode_grid_full(cols / 16, K), nullptr);
 }
@@ -828,6 +829,9 @@ exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M
     if ((st = check_ptr(R, "R", 4)) != EXL3_OK) return st;
     if (rows < 16 || cols < 16 || rows % 16 || cols % 16)
         return set_error(EXL3_ERR_UNSUPPORTED, "rows and cols must be positive multiples of 16");
+    if (rows > (1ll << 24) || cols > (1ll << 24) || rows * cols > (1ll << 34))
+        return set_error(EXL3_ERR_INVALID_ARG, "matrix %lldx%lld is too large", (long long)rows,
+                         (long long)cols);
     if ((st = check_ptr(M, "M", 4)) != EXL3_OK) return st;
     if ((st = check_k(K)) != EXL3_OK) return st;
     if (!(scale > 0.0f) || !std::isfinite(scale) || !std::isfinite(1.0f / scale))

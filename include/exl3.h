@@ -302,7 +302,8 @@ EXL3_API exl3_status exl3_block_ldl(const double *H, int64_t n, double sigma_reg
  * that minimises the Hessian-weighted error tr(E^T H E) span by span.
  * Codes come from fl32(U * fl32(1 / scale)), as in exl3_encode_tiles.
  *   R (device) float [rows, cols]: rotated weights with the input channels (the
- *     Hessian's index) down the rows; rows and cols multiples of 16.
+ *     Hessian's index) down the rows; rows and cols multiples of 16, each at
+ *     most 2^24, rows * cols at most 2^34.
  *   M (device) float [rows, rows]: from exl3_block_ldl (only the strictly
  *     lower block part is read).
  *   K in {1, 2, 3, 4}; scale > 0 and finite (e.g. fl32(g * sigma_R)).

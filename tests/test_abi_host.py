@@ -138,6 +138,7 @@ def test_ldl_and_ldlq_reject_bad_arguments(ex):
     lq = lambda rows=64, cols=128, K=2, s=1.0, w=wq, codes=FAKE: L.exl3_ldlq(
         FAKE, rows, cols, FAKE, K, ctypes.c_float(s), codes, None, FAKE, w, None)
     assert lq(rows=40) == 2 and lq(cols=8) == 2
+    assert lq(rows=1 << 20, cols=1 << 15) == 1             # 2^35 elements
     assert lq(K=5) == 2
     assert lq(s=0.0) == 1 and lq(s=float("nan")) == 1
     assert lq(codes=None) == 1
