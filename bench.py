@@ -44,12 +44,12 @@ def alg_ops_per_tile(K: int) -> float:
 ALU_LANES_PER_SM_CLK = 128
 SM_MAX_MHZ_NOMINAL = 2070.0
 
-# DRAM traffic of one encode launch per tile, from an ncu capture
-# (profiles/encode_k2_small.md); valid only for the source it was taken on.
+# DRAM traffic of one encode launch per tile, from an ncu capture; valid only
+# for the source it was taken on.
 ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
-    # `ncu --set full` on 1,216 tiles (profiles/encode_k2_small.md); the traffic is
-    # the decision rows, proportional to the tiles processed.
+    # `ncu --set full` on 1,216 tiles of N(0, 1) targets (profile case `encode`); the
+    # traffic is the decision rows, proportional to the tiles processed.
     "36bba21314bc4c80f2b5ddd9e4436322fd4c311bbc344bac8df95c1dbc57f75d": 1545546.0,
 }
 
