@@ -131,16 +131,17 @@ __global__ void __launch_bounds__(kPanelThreads) chol_panel_kernel(double *__res
 }
 
 // Trailing update after panel p0: A[i][j] -= L[i][p0+k] L[j][p0+k], k = 0..15
-// ascending, for p0 + 16 <= j <= i < n.  64 x 64 tiles on or below the
-// diagonal; thread (ty, tx) owns entries (ty + 16a, tx + 16b).
+// ascending, for start <= j <= i < n (start = p0 + 32: the next panel's 16
+// columns get the same terms from chol_strip_kernel).  64 x 64 tiles on or
+// below the diagonal; thread (ty, tx) owns entries (ty + 16a, tx + 16b).
 __global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ A, int64_t n,
-                                                          int64_t p0) {
+                                                          int64_t p0, int64_t start) {
     const int ti = blockIdx.y, tj = blockIdx.x;
     if (tj > ti)
         return;
     __shared__ double Li[kUpdTile][17], Lj[kUpdTile][17];
     const int t = threadIdx.x;
-    const int64_t p1 = p0 + 16;
+    const int64_t p1 = start;
     const int64_t i0 = p1 + (int64_t)kUpdTile * ti, j0 = p1 + (int64_t)kUpdTile * tj;
     for (int e = t; e < kUpdTile * 16; e += 256) {
         const int r = e >> 4, k = e & 15;
@@ -179,6 +180,24 @@ __global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ A
             if (gi < n && gj <= gi)
                 A[gi * n + gj] = acc[a][b];
         }
+}
+
+// The same update for the next panel's columns only: A[i][j] -= L[i][p0+k] L[j][p0+k],
+// k = 0..15 ascending, for p0 + 16 <= j < p0 + 32, j <= i < n; one entry per thread.
+__global__ void __launch_bounds__(256) chol_strip_kernel(double *__restrict__ A, int64_t n,
+                                                         int64_t p0) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = p0 + 16 + (idx >> 4);
+    const int64_t j = p0 + 16 + (idx & 15);
+    if (i >= n || j > i)
+        return;
+    const double *li = A + i * n + p0;
+    const double *lj = A + j * n + p0;
+    double acc = A[i * n + j];
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+        acc = __dsub_rn(acc, __dmul_rn(li[k], lj[k]));
+    A[i * n + j] = acc;
 }
 
 // M[i][16b + c] = fl32(sum_{k=c..15} L[i][16b+k] X[k][c]) for rows i >= 16(b+1),
@@ -296,29 +315,97 @@ __global__ void __launch_bounds__(256) ldlq_feedback_kernel(float *__restrict__ 
 
 }  // namespace
 
+namespace {
+
+// A second stream and the events that order it against the caller's stream,
+// created for one factorisation and released on every return path.
+struct Lookahead {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, panel[2] = {}, rest[2] = {};
+    exl3_status init() {
+        exl3_status st;
+        if ((st = cuda_check(cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking),
+                             "look-ahead stream")) != EXL3_OK)
+            return st;
+        cudaEvent_t *evs[6] = {&fork, &join, &panel[0], &panel[1], &rest[0], &rest[1]};
+        for (cudaEvent_t *e : evs)
+            if ((st = cuda_check(cudaEventCreateWithFlags(e, cudaEventDisableTiming),
+                                 "look-ahead event")) != EXL3_OK)
+                return st;
+        return EXL3_OK;
+    }
+    ~Lookahead() {
+        for (cudaEvent_t e : {fork, join, panel[0], panel[1], rest[0], rest[1]})
+            if (e)
+                cudaEventDestroy(e);
+        if (side)
+            cudaStreamDestroy(side);
+    }
+};
+
+}  // namespace
+
+// One attempt, with look-ahead: panel p + 1 (and the update of its own 16
+// columns by panel p) runs on a second stream while the caller's stream applies
+// panel p to everything to the right of them.  Each entry still receives its
+// terms in ascending k, so the factor is the same as without look-ahead.
+//   side:  panel(0) | strip(0) panel(1) | strip(1) panel(2) | ...
+//   main:           rest(0)             | rest(1)          | ...
+// rest(p) waits for panel(p); strip(p) waits for rest(p - 1), the last writer of
+// the columns it updates.
+static exl3_status cholesky_attempt(const BlockLdlLaunch &p, int a, Lookahead &la, cudaStream_t s) {
+    const int64_t n = p.n;
+    exl3_status st;
+    const int ix = (int)((n + 255) / 256 < 64 ? (n + 255) / 256 : 64);
+    chol_init_kernel<<<dim3(ix, (unsigned)n), 256, 0, s>>>(p.H, p.A, n, a, p.delta, p.flag);
+    note_launch();
+    if ((st = cuda_check(cudaEventRecord(la.fork, s), "fork")) != EXL3_OK) return st;
+    if ((st = cuda_check(cudaStreamWaitEvent(la.side, la.fork, 0), "fork wait")) != EXL3_OK) return st;
+    auto panel = [&](int64_t p0) {
+        const int64_t below = n - p0 - 16;
+        const unsigned gp = below > 0 ? (unsigned)((below + kPanelThreads - 1) / kPanelThreads) : 1u;
+        chol_panel_kernel<<<gp, kPanelThreads, 0, la.side>>>(p.A, p.LD + (p0 / 16) * 256, n, p0,
+                                                              p.flag);
+        note_launch();
+    };
+    panel(0);
+    if ((st = cuda_check(cudaEventRecord(la.panel[0], la.side), "panel event")) != EXL3_OK) return st;
+    for (int64_t q = 0; 16 * q + 16 < n; q++) {
+        const int64_t p0 = 16 * q;
+        const int64_t below = n - p0 - 16;             // rows under panel q (>= 16)
+        // main: panel q applied to the columns right of panel q + 1
+        if ((st = cuda_check(cudaStreamWaitEvent(s, la.panel[q & 1], 0), "panel wait")) != EXL3_OK)
+            return st;
+        if (below > 16) {
+            const unsigned T = (unsigned)((below - 16 + kUpdTile - 1) / kUpdTile);
+            chol_update_kernel<<<dim3(T, T), 256, 0, s>>>(p.A, n, p0, p0 + 32);
+            note_launch();
+        }
+        if ((st = cuda_check(cudaEventRecord(la.rest[q & 1], s), "rest event")) != EXL3_OK) return st;
+        // side: panel q applied to panel q + 1's columns, then panel q + 1
+        if (q > 0 && (st = cuda_check(cudaStreamWaitEvent(la.side, la.rest[(q - 1) & 1], 0),
+                                      "rest wait")) != EXL3_OK)
+            return st;
+        chol_strip_kernel<<<(unsigned)((below * 16 + 255) / 256), 256, 0, la.side>>>(p.A, n, p0);
+        note_launch();
+        panel(p0 + 16);
+        if ((st = cuda_check(cudaEventRecord(la.panel[(q + 1) & 1], la.side), "panel event")) != EXL3_OK)
+            return st;
+    }
+    if ((st = cuda_check(cudaEventRecord(la.join, la.side), "join")) != EXL3_OK) return st;
+    if ((st = cuda_check(cudaStreamWaitEvent(s, la.join, 0), "join wait")) != EXL3_OK) return st;
+    return cuda_check(cudaGetLastError(), "cholesky launch");
+}
+
 exl3_status run_block_ldl(const BlockLdlLaunch &p, cudaStream_t s) {
     const int64_t n = p.n;
     exl3_status st;
+    Lookahead la;
+    if ((st = la.init()) != EXL3_OK) return st;
     diag_delta_kernel<<<1, 1024, 0, s>>>(p.H, n, p.sigma_reg, p.delta);
     note_launch();
     for (int a = 0; a <= p.max_retries; a++) {
-        const int ix = (int)((n + 255) / 256 < 64 ? (n + 255) / 256 : 64);
-        chol_init_kernel<<<dim3(ix, (unsigned)n), 256, 0, s>>>(p.H, p.A, n, a, p.delta, p.flag);
-        note_launch();
-        for (int64_t p0 = 0; p0 < n; p0 += 16) {
-            const int64_t below = n - p0 - 16;
-            const unsigned gp =
-                below > 0 ? (unsigned)((below + kPanelThreads - 1) / kPanelThreads) : 1u;
-            chol_panel_kernel<<<gp, kPanelThreads, 0, s>>>(p.A, p.LD + (p0 / 16) * 256, n, p0,
-                                                           p.flag);
-            note_launch();
-            if (below > 0) {
-                const unsigned T = (unsigned)((below + kUpdTile - 1) / kUpdTile);
-                chol_update_kernel<<<dim3(T, T), 256, 0, s>>>(p.A, n, p0);
-                note_launch();
-            }
-        }
-        if ((st = cuda_check(cudaGetLastError(), "cholesky launch")) != EXL3_OK) return st;
+        if ((st = cholesky_attempt(p, a, la, s)) != EXL3_OK) return st;
         int failed = 0;
         if ((st = cuda_check(cudaMemcpyAsync(&failed, p.flag, sizeof(int), cudaMemcpyDeviceToHost, s),
                              "pivot flag copy")) != EXL3_OK)
