@@ -254,10 +254,11 @@ def test_quantize_small_workspace_same_result(ex):
     assert float(full["mse"].item()) == float(small["mse"].item())
 
 
-def test_gss_matches_oracle_search(ex):
-    rows, cols, K = 128, 128, 2
-    W = inputs.linear_bf16(rows, cols, seed=41, std=0.02)
-    su, sv = inputs.sign_pair(rows, cols, 41)
+@pytest.mark.parametrize("K,seed", [(2, 41), (1, 42), (3, 43), (4, 44)])
+def test_gss_matches_oracle_search(ex, K, seed):
+    rows, cols = 128, 128
+    W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02)
+    su, sv = inputs.sign_pair(rows, cols, seed)
     res = ex.gss_scale(W.to(DEV), su.to(DEV), sv.to(DEV), K, 0.5, 2.0, 12, want_history=True)
     torch.cuda.synchronize()
     Wf, sun, svn = W.float().numpy(), su.numpy(), sv.numpy()
@@ -424,7 +425,8 @@ def test_encode_rows_one_block_many_rows(ex):
 # grid-and-parabola scale search
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rows,cols,K,seed", [(128, 256, 2, 61), (256, 128, 3, 62), (128, 128, 4, 63)])
+@pytest.mark.parametrize("rows,cols,K,seed", [(128, 256, 2, 61), (256, 128, 3, 62), (128, 128, 4, 63),
+                                              (128, 128, 1, 64)])
 def test_scale_search_matches_oracle(ex, rows, cols, K, seed):
     from oracle import scale_search as ss
     W = inputs.linear_bf16(rows, cols, seed=seed, std=0.02, outlier_frac=0.002)
