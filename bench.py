@@ -276,6 +276,8 @@ def run_ours(args):
     peaks, peak_kind = _peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     f_max = float(peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL))
+    clock_src = ("sm_max_mhz of MEASURED_PEAKS.json" if "sm_max_mhz" in peaks and peak_kind == "measured"
+                 else "the recipe's maximum SM clock")
     peak_tops = sms * ALU_LANES_PER_SM_CLK * f_max * 1e6 / 1e12
     enc_launch_s = (enc_ms / max(enc_n, 1)) / 1e3
     ops_launch = alg_ops_per_tile(K) * n_tiles
@@ -287,7 +289,7 @@ def run_ours(args):
                 "traffic": (tpt * n_tiles) if tpt is not None else None,
                 "kernel": "encode_kernel<2>",
                 "peak_basis": f"{sms} SMs x {ALU_LANES_PER_SM_CLK} lane-ops/clk x {f_max:.0f} MHz "
-                              f"(max SM clock, {peak_kind})",
+                              f"(ALU-bound: unit counts x clock, clock from {clock_src})",
                 "alg_ops_per_tile": alg_ops_per_tile(K),
                 "encode_ms_per_launch": enc_launch_s * 1e3,
                 "encode_share_of_step": (enc_ms / 1e3) / tot_s}
@@ -320,8 +322,10 @@ def run_ours(args):
     rot_bytes = rows * cols * (2 + 4)
     rot_gbs = rot_bytes / (statistics.median(rot_ms) / 1e3) / 1e9
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = ("of measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks and peak_kind == "measured"
+               else "of fallback (the recipe's 6.8 TB/s)")
     rotation = {"bound": "hbm", "achieved": rot_gbs, "peak": hbm_peak, "unit": "GB/s",
-                "frac": rot_gbs / hbm_peak, "bytes_per_launch": rot_bytes,
+                "frac": rot_gbs / hbm_peak, "peak_source": hbm_src, "bytes_per_launch": rot_bytes,
                 "ms_per_launch": statistics.median(rot_ms),
                 "l2": "4 copies of the workload rotated in turn (384 MiB > L2), no flush"}
 
