@@ -731,3 +731,34 @@ def test_quantize_and_gss_replay_from_cuda_graph(ex, K):
         assert float(gs["g"].item()) == float(gdirect["g"].item())
         codes.zero_()
         gcodes.zero_()
+
+
+def test_ldlq_scale_search_regularize_replay_from_cuda_graph(ex):
+    """The other asynchronous entry points capture and replay bit for bit too
+    (exl3_block_ldl reads a device flag back and is called outside the graph)."""
+    n, cols, K = 128, 256, 2
+    H = inputs.spd_hessian(n, 91, rho=0.95).to(DEV)
+    M, _ = ex.block_ldl(H)
+    R = inputs.iid_f32(n, cols, 92).to(DEV)
+    W = inputs.linear_bf16(n, cols, seed=93).to(DEV)
+    su, sv = (t.to(DEV) for t in inputs.sign_pair(n, cols, 93))
+    h = inputs.hessian_diag(n, 94).to(DEV)
+    wl = torch.empty(ex.ldlq_workspace_bytes(n, cols, K), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(ex.scale_search_workspace_bytes(n, cols, K), dtype=torch.uint8, device=DEV)
+    wr = torch.empty(ex.regularize_workspace_bytes(n, cols), dtype=torch.uint8, device=DEV)
+    d_lq = ex.ldlq(R, M, K, 0.9, ws=wl)
+    d_ss = ex.scale_search(W, su, sv, K, ws=ws)
+    d_rg = ex.regularize(W, h, sv, ws=wr)
+    torch.cuda.synchronize()
+    codes = torch.zeros_like(d_lq["codes"])
+    Wout = torch.zeros_like(d_rg["W_out"])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        lq = ex.ldlq(R, M, K, 0.9, codes=codes, ws=wl)
+        ss = ex.scale_search(W, su, sv, K, ws=ws)
+        rg = ex.regularize(W, h, sv, W_out=Wout, ws=wr)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(codes, d_lq["codes"]) and torch.equal(lq["Q"], d_lq["Q"])
+    assert torch.equal(ss["history"], d_ss["history"])
+    assert torch.equal(Wout, d_rg["W_out"]) and torch.equal(rg["sv_out"], d_rg["sv_out"])
