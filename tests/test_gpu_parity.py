@@ -762,3 +762,30 @@ def test_ldlq_scale_search_regularize_replay_from_cuda_graph(ex):
     assert torch.equal(codes, d_lq["codes"]) and torch.equal(lq["Q"], d_lq["Q"])
     assert torch.equal(ss["history"], d_ss["history"])
     assert torch.equal(Wout, d_rg["W_out"]) and torch.equal(rg["sv_out"], d_rg["sv_out"])
+
+
+def test_concurrent_streams_do_not_interfere(ex):
+    """Two quantize calls (K=2 and K=1) enqueued on two streams at once, each with
+    its own workspace, give the results of the same calls made one after the
+    other: the library keeps no device state outside the caller's buffers."""
+    mats = []
+    for seed, K in ((101, 2), (102, 1)):
+        W = inputs.linear_bf16(256, 256, seed=seed).to(DEV)
+        su, sv = (t.to(DEV) for t in inputs.sign_pair(256, 256, seed))
+        ws = torch.empty(ex.quantize_workspace_bytes(256, 256, K), dtype=torch.uint8, device=DEV)
+        mats.append((W, su, sv, K, ws))
+    seq = [ex.quantize(W, su, sv, K, 1.0, ws=ws) for W, su, sv, K, ws in mats]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    par = []
+    for rep in range(3):
+        outs = []
+        for st, (W, su, sv, K, ws) in zip(streams, mats):
+            with torch.cuda.stream(st):
+                outs.append(ex.quantize(W, su, sv, K, 1.0, ws=ws))
+        torch.cuda.synchronize()
+        par.append(outs)
+    for outs in par:
+        for a, b in zip(outs, seq):
+            assert torch.equal(a["codes"], b["codes"])
+            assert float(a["mse"].item()) == float(b["mse"].item())
