@@ -155,3 +155,36 @@ def test_planted_mistakes_are_caught_by_enumeration():
                 found_tie_case = True
                 break
     assert found_tie_case
+
+
+def test_random_trellises_match_enumeration():
+    """Randomised breadth for the enumeration pins: random state widths, bits per
+    step, lengths, codebooks (continuous or small integers, so ties occur) and
+    targets; the oracle's tracked final row equals the best enumerated path into
+    every group, and its traced path has the minimal cost."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(L=st.integers(3, 6), K=st.integers(1, 3), T=st.integers(2, 6),
+               seed=st.integers(0, 2**31 - 1), integer=st.booleans())
+    def check(L, K, T, seed, integer):
+        hyp.assume(K < L and (1 << L) * (1 << (K * (T - 1))) <= 1 << 14)
+        rng = np.random.default_rng(seed)
+        if integer:
+            cb = rng.integers(-3, 4, 1 << L).astype(np.float32)
+            y = rng.integers(-3, 4, T).astype(np.float32)
+        else:
+            cb = rng.standard_normal(1 << L).astype(np.float32)
+            y = rng.standard_normal(T).astype(np.float32)
+        dec, fc, pen = oracle.viterbi_forward(y, L, K, cb, constrained=False)
+        paths = all_paths(L, K, T)
+        costs = path_costs(paths, y, cb)
+        low = (1 << (L - K)) - 1
+        for g in range(1 << (L - K)):
+            assert fc[g] == costs[(paths[:, -1] & low) == g].min()
+        s_star = oracle.final_argmin(dec[-1], fc, L, K)
+        stt = oracle.traceback(dec, L, K, T - 1, 0, s_star)
+        assert path_costs(stt[None, :].astype(np.int64), y, cb)[0] == costs.min()
+
+    check()
