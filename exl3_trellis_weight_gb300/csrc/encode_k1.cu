@@ -5,19 +5,21 @@
 // not fit one SM's shared memory.  A tile is therefore encoded by a cluster of
 // two 1024-thread blocks on two SMs.  Unit h' (tracked entries 2h', 2h'+1)
 // reads M(h') and M(16384 + h'); block r handles the 8192 units
-// h' = r*8192 + u*1024 + tid (u = 0..7) and keeps, double-buffered in its
-// shared memory, exactly the costs its units read:
+// h' = r*8192 + u2*2048 + 2*tid + m (u2 = 0..3, m = 0, 1: adjacent pairs, so
+// the two costs each array read are one 8-byte load) and keeps, double-buffered
+// in its shared memory, exactly the costs its units read:
 //   A[i] = M(r*8192 + i),  B[i] = M(16384 + r*8192 + i),  i in [0, 8192).
-// The writer pushes: entry g = 2h' + j produced by block r is read next step by
-// block (g >> 13) & 1 (= u >> 2) as its A (r = 0) or B (r = 1) value at index
-// g & 8191, so units u < 4 store into block 0 and u >= 4 into block 1 (plain
-// st.shared::cluster through the mapped address; no multicast).  Every read is
-// local.  One cluster barrier separates consecutive steps; its release orders
-// the pushed stores before the peer's reads.
+// The writer pushes: a unit pair yields the four entries
+// g = 4 (r*4096 + u2*1024 + tid) + 0..3, read next step by block (g >> 13) & 1
+// (= u2 >> 1) as its A (r = 0) or B (r = 1) values at g & 8191 -- one 16-byte
+// store, into the own block or the peer's (plain st.shared::cluster through
+// the mapped address; no multicast).  Every read is local.  One cluster barrier
+// separates consecutive steps; its release orders the pushed stores before the
+// peer's reads.
 //
 // Everything else follows encode.cu: the same two passes, tie rules, packing,
 // 1024-word decision rows (each block writes the rows of its own entries into
-// its own workspace slice: word tid, bit 2u + j), and the same two-tile
+// its own workspace slice: word tid, bit 4 u2 + 2 m + j), and the same two-tile
 // pipeline with an interleaved traceback run by thread 0 of block 0.
 #include <cooperative_groups.h>
 
@@ -59,9 +61,10 @@ __device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const f
 // Where D_t(g) of tracked entry g (15 bits) lives: owner block, word, bit.
 __device__ __forceinline__ void k1_locate(uint32_t g, int &owner, int &word, int &bit) {
     const uint32_t hp = g >> 1;
+    const uint32_t i = hp & 8191u;               // u2 * 2048 + 2 tid + m
     owner = (int)(hp >> 13);
-    word = (int)(hp & 1023u);
-    bit = (int)(((hp >> 10) & 7u) * 2u + (g & 1u));
+    word = (int)((i >> 1) & 1023u);
+    bit = (int)((i >> 11) * 4u + (i & 1u) * 2u + (g & 1u));
 }
 
 // traceback step helpers (thread 0 of block 0); tb.rows = slot rows in block 0's slice
@@ -85,8 +88,9 @@ __device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
         tb.on = false;
 }
 
-// One step of block r: 8 units x 2 entries x 2 candidates per thread.  The
-// squares q[u*2 + k] (entries 2h', 2h'+1 of unit u, candidate k) were computed
+// One step of block r: 4 unit pairs x 2 units x 2 entries x 2 candidates per
+// thread.  The squares q[u*2 + k] (unit u = 2 u2 + m, entries 2h', 2h'+1,
+// candidate k) were computed
 // beforehand (they do not depend on the cost row).  A, B: this block's read
 // buffer; dst0 / dst1: the next-step array of block 0 / block 1 this block
 // writes into (its own or the peer's, mapped).
@@ -97,32 +101,43 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
                                         const int tid, uint32_t &word, unsigned long long &key) {
     word = 0u;
 #pragma unroll
-    for (int u = 0; u < 8; u++) {
-        const int i = u * 1024 + tid;
-        const float m0 = A[i];   // M(h')
-        const float m1 = B[i];   // M(16384 + h')
-        const unsigned long long q0 = q[u * 2 + 0], q1 = q[u * 2 + 1];
-        int best0 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 & 0xffffffffull))));
-        int best1 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 >> 32))));
-        const int c0 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 & 0xffffffffull))));
-        const int c1 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 >> 32))));
-        bool keep0, keep1;
-        best0 = __vibmin_s32(best0, c0, &keep0);   // ties keep k = 0
-        best1 = __vibmin_s32(best1, c1, &keep1);
-        const uint32_t bk0 = keep0 ? 0u : 1u, bk1 = keep1 ? 0u : 1u;
-        word |= (bk0 << (2 * u)) | (bk1 << (2 * u + 1));
-        if (ARGMIN) {
-            const uint32_t g0 = 2u * (uint32_t)(r * 8192 + i);
-            const unsigned long long k0 =
-                ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << 15) | g0);
-            const unsigned long long k1 =
-                ((unsigned long long)(uint32_t)best1 << 32) | ((bk1 << 15) | (g0 + 1u));
-            key = k0 < key ? k0 : key;
-            key = k1 < key ? k1 : key;
-        } else {
-            float *dst = (u < 4) ? dst0 : dst1;
-            *reinterpret_cast<float2 *>(dst + 2 * ((u & 3) * 1024 + tid)) =
-                make_float2(__int_as_float(best0), __int_as_float(best1));
+    for (int u2 = 0; u2 < 4; u2++) {
+        const int i = u2 * 2048 + 2 * tid;        // units h' = r*8192 + i, i + 1
+        const float2 ma = *reinterpret_cast<const float2 *>(A + i);
+        const float2 mb = *reinterpret_cast<const float2 *>(B + i);
+        float out[4];
+#pragma unroll
+        for (int m = 0; m < 2; m++) {
+            const float m0 = m ? ma.y : ma.x;      // M(h')
+            const float m1 = m ? mb.y : mb.x;      // M(16384 + h')
+            const int u = 2 * u2 + m;
+            const unsigned long long q0 = q[u * 2 + 0], q1 = q[u * 2 + 1];
+            int best0 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 & 0xffffffffull))));
+            int best1 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 >> 32))));
+            const int c0 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 & 0xffffffffull))));
+            const int c1 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 >> 32))));
+            bool keep0, keep1;
+            best0 = __vibmin_s32(best0, c0, &keep0);   // ties keep k = 0
+            best1 = __vibmin_s32(best1, c1, &keep1);
+            const uint32_t bk0 = keep0 ? 0u : 1u, bk1 = keep1 ? 0u : 1u;
+            word |= (bk0 << (4 * u2 + 2 * m)) | (bk1 << (4 * u2 + 2 * m + 1));
+            if (ARGMIN) {
+                const uint32_t g0 = 2u * (uint32_t)(r * 8192 + i + m);
+                const unsigned long long k0 =
+                    ((unsigned long long)(uint32_t)best0 << 32) | ((bk0 << 15) | g0);
+                const unsigned long long k1 =
+                    ((unsigned long long)(uint32_t)best1 << 32) | ((bk1 << 15) | (g0 + 1u));
+                key = k0 < key ? k0 : key;
+                key = k1 < key ? k1 : key;
+            }
+            out[2 * m] = __int_as_float(best0);
+            out[2 * m + 1] = __int_as_float(best1);
+        }
+        if (!ARGMIN) {
+            // entries 4 (r*4096 + u2*1024 + tid) + 0..3: read next step by block u2 >> 1
+            float *dst = (u2 < 2) ? dst0 : dst1;
+            *reinterpret_cast<float4 *>(dst + (u2 & 1) * 4096 + 4 * tid) =
+                make_float4(out[0], out[1], out[2], out[3]);
         }
     }
 }
@@ -163,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int u = 0; u < 8; u++)
 #pragma unroll
         for (int k = 0; k < 2; k++) {
-            const uint32_t hp = (uint32_t)(r * 8192 + u * 1024 + tid);
+            const uint32_t hp = (uint32_t)(r * 8192 + (u >> 1) * 2048 + 2 * tid + (u & 1));
             const uint32_t s0 = ((uint32_t)k << 15) | (2u * hp);
             vpk[u * 2 + k] = (uint32_t)__half_as_ushort(mul1_half(s0)) |
                              ((uint32_t)__half_as_ushort(mul1_half(s0 + 1u)) << 16);
