@@ -498,6 +498,30 @@ def run_ours(args):
                              "skew": float(rr["info"][0].item())}
         del W_o, ws_r, h_d
 
+        # the same 4096x4096 step at K=1 (two-block clusters per tile)
+        ws_1 = torch.empty(ex.quantize_workspace_bytes(rows, cols, 1), dtype=torch.uint8, device=dev)
+        codes_1 = torch.empty(rows // 16, cols // 16, 16, dtype=torch.int16, device=dev)
+        ex.quantize(W, su, sv, 1, 1.0, codes=codes_1, ws=ws_1)
+        torch.cuda.synchronize(dev)
+        ex.profile_enable(True)
+        k1_ms = []
+        for _ in range(2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex.quantize(W, su, sv, 1, 1.0, codes=codes_1, ws=ws_1)
+            b.record(stream)
+            b.synchronize()
+            k1_ms.append(a.elapsed_time(b))
+        e1_ms, e1_n, _ = ex.profile_read()
+        ex.profile_enable(False)
+        ach1 = alg_ops_per_tile(1) * n_tiles / ((e1_ms / max(e1_n, 1)) / 1e3) / 1e12
+        aux["k1"] = {"ms": sum(k1_ms) / len(k1_ms),
+                     "tiles_per_s": n_tiles * len(k1_ms) / (sum(k1_ms) / 1e3),
+                     "roofline_frac": ach1 / peak_tops,
+                     "workload": "linear4096_k2's matrix at K=1 (76 two-block clusters)"}
+        del ws_1, codes_1
+
         # the 12-evaluation golden-section search on 4096x4096 K=2 (12 quantize passes)
         (_, Wg, sug, svg, Kg), = inputs.workload("gss4096_k2")
         Wg, sug, svg = Wg.to(dev), sug.to(dev), svg.to(dev)

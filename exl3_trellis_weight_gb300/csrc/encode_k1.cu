@@ -94,14 +94,18 @@ __device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
 // beforehand (they do not depend on the cost row).  A, B: this block's read
 // buffer; dst0 / dst1: the next-step array of block 0 / block 1 this block
 // writes into (its own or the peer's, mapped).
-template <bool ARGMIN>
+// FIRST: the pair processed first (2 for block 0, 0 for block 1), so the pairs
+// whose costs go to the peer block are computed and pushed first and their
+// remote stores have the longest time to land before the barrier's release.
+template <bool ARGMIN, int FIRST>
 __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float *__restrict__ B,
                                         float *dst0, float *dst1,
                                         const unsigned long long (&q)[16], const int r,
                                         const int tid, uint32_t &word, unsigned long long &key) {
     word = 0u;
 #pragma unroll
-    for (int u2 = 0; u2 < 4; u2++) {
+    for (int sidx = 0; sidx < 4; sidx++) {
+        const int u2 = (sidx + FIRST) & 3;
         const int i = u2 * 2048 + 2 * tid;        // units h' = r*8192 + i, i + 1
         const float2 ma = *reinterpret_cast<const float2 *>(A + i);
         const float2 mb = *reinterpret_cast<const float2 *>(B + i);
@@ -309,7 +313,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *const *Wn = (t & 1) ? W0 : W1;
                 uint32_t word;
                 unsigned long long key = 0ull;
-                k1_step<false>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
+                if (r == 0)
+                    k1_step<false, 2>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
+                else
+                    k1_step<false, 0>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
                 // publish this step's costs, then do the work that needs no peer
                 // data (next squares, decision store, traceback) before waiting
                 cluster_arrive();
@@ -326,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     k1_tb_issue(tb);
                 uint32_t word;
                 unsigned long long key = ~0ull;
-                k1_step<true>(A1, B1, nullptr, nullptr, q, r, tid, word, key);
+                k1_step<true, 0>(A1, B1, nullptr, nullptr, q, r, tid, word, key);
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
                 key = warp_min_u64(key);
