@@ -519,6 +519,7 @@ def run_ours(args):
         aux["k1"] = {"ms": sum(k1_ms) / len(k1_ms),
                      "tiles_per_s": n_tiles * len(k1_ms) / (sum(k1_ms) / 1e3),
                      "roofline_frac": ach1 / peak_tops,
+                     "wait_timeouts": ex.wait_timeouts(),   # nonzero: the K=1 results are void
                      "workload": "linear4096_k2's matrix at K=1 (76 two-block clusters)"}
         del ws_1, codes_1
 

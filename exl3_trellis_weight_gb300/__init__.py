@@ -21,7 +21,7 @@ __all__ = [
     "encode_rows", "decode_rows",
     "quantize", "gss_scale", "scale_search", "scale_search_workspace_bytes", "encode_workspace_bytes", "encode_workspace_min_bytes",
     "quantize_workspace_bytes", "gss_workspace_bytes", "mse_workspace_bytes",
-    "supports_k", "profile_enable", "profile_read", "EXL3_F32", "EXL3_BF16",
+    "supports_k", "profile_enable", "profile_read", "wait_timeouts", "EXL3_F32", "EXL3_BF16",
 ]
 
 EXL3_F32 = 0
@@ -95,7 +95,8 @@ def lib():
         L.exl3_profile_enable.argtypes = [i32]
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
-        for name in ("exl3_regularize", "exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
+        L.exl3_wait_timeouts.argtypes = [P]
+        for name in ("exl3_regularize", "exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_wait_timeouts", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
         _lib = L
@@ -164,6 +165,17 @@ def profile_read():
     nk = ctypes.c_int64(0)
     _check(lib().exl3_profile_read(ctypes.byref(ms), ctypes.byref(ne), ctypes.byref(nk)))
     return ms.value, ne.value, nk.value
+
+
+def wait_timeouts() -> int:
+    """exl3_wait_timeouts -> number of bounded device waits (K=1 encoder) that
+    expired since the last call; synchronises the device and resets the count.
+    A nonzero count means the launches concerned produced void results."""
+    n = ctypes.c_uint(0)
+    st = lib().exl3_wait_timeouts(ctypes.byref(n))
+    if st not in (0, 6):
+        _check(st)
+    return int(n.value)
 
 
 def supports_k(K: int) -> bool:

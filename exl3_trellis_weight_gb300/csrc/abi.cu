@@ -397,6 +397,7 @@ const char *exl3_status_str(int status) {
     case EXL3_ERR_WORKSPACE: return "EXL3_ERR_WORKSPACE";
     case EXL3_ERR_CUDA: return "EXL3_ERR_CUDA";
     case EXL3_ERR_NUMERIC: return "EXL3_ERR_NUMERIC";
+    case EXL3_ERR_TIMEOUT: return "EXL3_ERR_TIMEOUT";
     default: return "EXL3_ERR_UNKNOWN";
     }
 }
@@ -962,3 +963,13 @@ exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launches, int64
 }
 
 }  // extern "C"
+
+exl3_status exl3_wait_timeouts(unsigned int *count_out) {
+    unsigned int n = 0;
+    const exl3_status st = exl3::k1_take_wait_timeouts(&n);
+    if (count_out)
+        *count_out = n;
+    if (st != EXL3_OK)
+        return st;
+    return n ? exl3::set_error(EXL3_ERR_TIMEOUT, "%u device waits expired", n) : EXL3_OK;
+}

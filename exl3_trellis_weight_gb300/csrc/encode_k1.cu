@@ -6,21 +6,30 @@
 // two 1024-thread blocks on two SMs.  Unit h' (tracked entries 2h', 2h'+1)
 // reads M(h') and M(16384 + h'); block r handles the 8192 units
 // h' = r*8192 + u2*2048 + 2*tid + m (u2 = 0..3, m = 0, 1: adjacent pairs, so
-// the two costs each array read are one 8-byte load) and keeps, double-buffered
-// in its shared memory, exactly the costs its units read:
+// the two costs each array read are one 8-byte load) and keeps, in three
+// rotating buffers in its shared memory, exactly the costs its units read:
 //   A[i] = M(r*8192 + i),  B[i] = M(16384 + r*8192 + i),  i in [0, 8192).
 // The writer pushes: a unit pair yields the four entries
 // g = 4 (r*4096 + u2*1024 + tid) + 0..3, read next step by block (g >> 13) & 1
 // (= u2 >> 1) as its A (r = 0) or B (r = 1) values at g & 8191 -- one 16-byte
-// store, into the own block or the peer's (plain st.shared::cluster through
-// the mapped address; no multicast).  Every read is local.  One cluster barrier
-// separates consecutive steps; its release orders the pushed stores before the
-// peer's reads.
+// store, a plain shared store into the own block or an st.async into the
+// peer's that completes 16 bytes of the transaction count of the peer's
+// barrier for that buffer (no multicast).  Every read is local.
+//
+// Step t reads buffer t mod 3 and writes buffer (t+1) mod 3; it ends with the
+// block barrier (own stores) and a wait on the own transaction barrier of the
+// written buffer (the peer's 32 KiB).  No fence is needed: the buffer a push
+// of step t overwrites was last read at step t-2, and the pusher only got to
+// step t after the peer's step t-1 pushes had all arrived, each made after
+// the peer's block barrier that closed step t-2.  Each wait is bounded in time;
+// on expiry the block stops waiting, the results are void and a device flag
+// records it (exl3_k1_wait_timeouts).
 //
 // Everything else follows encode.cu: the same two passes, tie rules, packing,
 // 1024-word decision rows (each block writes the rows of its own entries into
 // its own workspace slice: word tid, bit 4 u2 + 2 m + j), and the same two-tile
-// pipeline with an interleaved traceback run by thread 0 of block 0.
+// pipeline with an interleaved traceback run by thread 0 of block 0; cluster
+// barriers separate the pipeline's phases.
 #include <cooperative_groups.h>
 
 #include "encode_common.cuh"
@@ -33,15 +42,69 @@ namespace {
 
 constexpr size_t kBlockWords = kEncodeBlockScratchBytes / sizeof(uint32_t);
 
+constexpr int kBufFloats = 16384;                    // one buffer: A[8192], B[8192]
+constexpr uint32_t kPushBytes = kThreads * 2u * 16u;  // bytes a block receives per step
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// number of K=1 barrier waits that gave up (read and cleared by the host)
+__device__ unsigned int g_k1_wait_timeouts;
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
 }
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// the same shared-memory offset in block `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// 16-byte store into a peer block, completing 16 bytes of its barrier's transaction
+__device__ __forceinline__ void push_peer(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void bar_init(uint32_t a) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(a) : "memory");
+}
+// the single arrival of a phase, announcing the bytes the phase waits for
+__device__ __forceinline__ void bar_expect(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_test(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    return ok != 0u;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of parity `parity` of the barrier at a.  Gives up after
+// kWaitLimitNs, or at once when another thread of the block already gave up.
+__device__ __noinline__ void bar_wait_slow(uint32_t a, uint32_t parity, volatile int *gave_up) {
+    const unsigned long long t0 = global_ns();
+    while (!bar_test(a, parity)) {
+        if (*gave_up)
+            return;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *gave_up = 1;
+            atomicAdd(&g_k1_wait_timeouts, 1u);
+            return;
+        }
+    }
+}
+__device__ __forceinline__ void bar_wait(uint32_t a, uint32_t parity, volatile int *gave_up) {
+    if (!bar_test(a, parity))
+        bar_wait_slow(a, parity, gave_up);
 }
 
 // fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair
@@ -90,16 +153,16 @@ __device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
 
 // One step of block r: 4 unit pairs x 2 units x 2 entries x 2 candidates per
 // thread.  The squares q[u*2 + k] (unit u = 2 u2 + m, entries 2h', 2h'+1,
-// candidate k) were computed
-// beforehand (they do not depend on the cost row).  A, B: this block's read
-// buffer; dst0 / dst1: the next-step array of block 0 / block 1 this block
-// writes into (its own or the peer's, mapped).
+// candidate k) were computed beforehand (they do not depend on the cost row).
+// A, B: this block's read buffer.  own: the array this block writes in its own
+// next buffer; peer / peer_bar: the same array in the peer's next buffer and
+// the peer's barrier for it (shared::cluster addresses).
 // FIRST: the pair processed first (2 for block 0, 0 for block 1), so the pairs
-// whose costs go to the peer block are computed and pushed first and their
-// remote stores have the longest time to land before the barrier's release.
+// whose costs go to the peer block (sidx 0, 1) are computed and pushed first
+// and have the longest time to land.
 template <bool ARGMIN, int FIRST>
 __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float *__restrict__ B,
-                                        float *dst0, float *dst1,
+                                        float *own, const uint32_t peer, const uint32_t peer_bar,
                                         const unsigned long long (&q)[16], const int r,
                                         const int tid, uint32_t &word, unsigned long long &key) {
     word = 0u;
@@ -139,9 +202,13 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
         }
         if (!ARGMIN) {
             // entries 4 (r*4096 + u2*1024 + tid) + 0..3: read next step by block u2 >> 1
-            float *dst = (u2 < 2) ? dst0 : dst1;
-            *reinterpret_cast<float4 *>(dst + (u2 & 1) * 4096 + 4 * tid) =
-                make_float4(out[0], out[1], out[2], out[3]);
+            // at array offset (u2 & 1) * 4096 + 4 tid
+            const int off = (u2 & 1) * 4096 + 4 * tid;
+            const float4 v = make_float4(out[0], out[1], out[2], out[3]);
+            if (sidx < 2)
+                push_peer(peer + 4u * (uint32_t)off, v, peer_bar);
+            else
+                *reinterpret_cast<float4 *>(own + off) = v;
         }
     }
 }
@@ -159,22 +226,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
     extern __shared__ __align__(16) unsigned char smem[];
-    // read buffers: buf b holds A_b[8192] then B_b[8192]
-    float *A0 = reinterpret_cast<float *>(smem);
-    float *B0 = A0 + 8192;
-    float *A1 = B0 + 8192;
-    float *B1 = A1 + 8192;
-    float *ys = B1 + 8192;
+    // cost buffers b = 0, 1, 2: A_b[8192] then B_b[8192]
+    float *const buf = reinterpret_cast<float *>(smem);
+    float *const A0 = buf;
+    float *const B0 = buf + 8192;
+    float *ys = buf + 3 * kBufFloats;
     uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
     __shared__ uint32_t sh_sstar[2], sh_end[2];
     __shared__ unsigned long long sh_key;
     __shared__ Tb tb;
-    // arrays this block writes: its A (r = 0) or B (r = 1) slot, in both blocks
-    float *const own0 = r == 0 ? A0 : B0;
-    float *const own1 = r == 0 ? A1 : B1;
-    float *const W0[2] = {cluster.map_shared_rank(own0, 0), cluster.map_shared_rank(own0, 1)};
-    float *const W1[2] = {cluster.map_shared_rank(own1, 0), cluster.map_shared_rank(own1, 1)};
+    __shared__ __align__(8) unsigned long long bars[3];   // transaction barrier per buffer
+    __shared__ int gave_up;
+    // the array this block writes (its A for r = 0, B for r = 1) in its own
+    // buffer 0, the same array in the peer's buffer 0, the barriers
+    const int own_off = r == 0 ? 0 : 8192;
+    const uint32_t peer_rank = (uint32_t)(r ^ 1);
+    const uint32_t peer0 = cluster_addr(smem_addr(buf + own_off), peer_rank);
+    const uint32_t bar0 = smem_addr(&bars[0]);
+    const uint32_t peer_bar0 = cluster_addr(bar0, peer_rank);
 
     const int tid = threadIdx.x;
     uint32_t vpk[16];
@@ -212,8 +282,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tb.s = tb.pending = 0u;
         tb.t = tb.stop = tb.row0 = tb.pass = tb.slot = 0;
         sh_end[0] = sh_end[1] = sh_sstar[0] = sh_sstar[1] = 0u;
+        gave_up = 0;
+        for (int b = 0; b < 3; b++)
+            bar_init(bar0 + 8u * (uint32_t)b);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // the peer's barriers are initialised before any push reaches them
     cluster_sync();
+    uint32_t parity = 0u;   // bit b: parity of the next phase of barrier b
 
     const int npairs = (n_my + 1) / 2;
     for (int ph = 0; ph <= npairs * 4; ph++) {
@@ -305,35 +381,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int row0 = (f_pass == 1) ? half - 1 : 0;
             unsigned long long q[16];
             k1_squares(vpk, ys[0], q);
+            int cur = 0;            // buffer read by step t: t mod 3
             for (int t = 0; t < T - 1; t++) {
+                const int nxt = cur == 2 ? 0 : cur + 1;
+                const uint32_t bar = bar0 + 8u * (uint32_t)nxt;
+                if (tid == 0)
+                    bar_expect(bar, kPushBytes);
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_issue(tb);
-                const float *Ap = (t & 1) ? A1 : A0;
-                const float *Bp = (t & 1) ? B1 : B0;
-                float *const *Wn = (t & 1) ? W0 : W1;
+                const float *Ap = buf + cur * kBufFloats;
+                float *own = buf + nxt * kBufFloats + own_off;
+                const uint32_t peer = peer0 + (uint32_t)(nxt * kBufFloats * 4);
+                const uint32_t peer_bar = peer_bar0 + 8u * (uint32_t)nxt;
                 uint32_t word;
                 unsigned long long key = 0ull;
                 if (r == 0)
-                    k1_step<false, 2>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
+                    k1_step<false, 2>(Ap, Ap + 8192, own, peer, peer_bar, q, r, tid, word, key);
                 else
-                    k1_step<false, 0>(Ap, Bp, Wn[0], Wn[1], q, r, tid, word, key);
-                // publish this step's costs, then do the work that needs no peer
-                // data (next squares, decision store, traceback) before waiting
-                cluster_arrive();
+                    k1_step<false, 0>(Ap, Ap + 8192, own, peer, peer_bar, q, r, tid, word, key);
+                // work that needs no new costs: next squares, decision store, traceback
                 k1_squares(vpk, ys[t + 1], q);
                 if (t >= row0)
                     rows[(size_t)(t - row0) * kRowWords + tid] = word;
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
-                cluster_wait();
+                __syncthreads();                                  // own stores
+                bar_wait(bar, (parity >> nxt) & 1u, &gave_up);    // the peer's pushes
+                parity ^= 1u << nxt;
+                cur = nxt;
             }
             if (f_pass == 1) {
-                // last step (T even: reads M_{T-2} from buffer 1); q holds its squares
+                // last step (reads M_{T-2} from buffer cur); q holds its squares
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_issue(tb);
                 uint32_t word;
                 unsigned long long key = ~0ull;
-                k1_step<true, 0>(A1, B1, nullptr, nullptr, q, r, tid, word, key);
+                const float *Ap = buf + cur * kBufFloats;
+                k1_step<true, 0>(Ap, Ap + 8192, nullptr, 0u, 0u, q, r, tid, word, key);
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
                 key = warp_min_u64(key);
@@ -351,14 +435,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const unsigned long long kk = sh_key < k1 ? sh_key : k1;
                     sh_sstar[f_slot] = (uint32_t)(kk & 0xffffffffull);
                 }
-            } else if (r == 0 && tid == 0 && a.tile_cost) {
-                // fl(M_{T-2}(end >> 1) + q_{T-1}(end)); M_{T-2} is in buffer 1 of the
-                // block that reads it: block (ge >> 13) & 1, array A/B by ge >> 14
-                const uint32_t e = sh_end[f_slot];
-                const uint32_t ge = e >> 1;
-                const float *arr = cluster.map_shared_rank((ge >> 14) ? B1 : A1, (int)((ge >> 13) & 1u));
-                const float d = __fsub_rn(ys[T - 1], mul1_value(e));
-                a.tile_cost[f_tile] = __fadd_rn(arr[ge & 8191u], __fmul_rn(d, d));
+            } else if (a.tile_cost) {
+                // fl(M_{T-2}(end >> 1) + q_{T-1}(end)); M_{T-2} is in buffer cur of the
+                // block that reads it: block (ge >> 13) & 1, array A/B by ge >> 14.
+                // The cluster barrier makes both blocks' last stores visible.
+                cluster_sync();
+                if (r == 0 && tid == 0) {
+                    const uint32_t e = sh_end[f_slot];
+                    const uint32_t ge = e >> 1;
+                    const float *Ac = buf + cur * kBufFloats;
+                    const float *arr =
+                        cluster.map_shared_rank((ge >> 14) ? Ac + 8192 : Ac, (int)((ge >> 13) & 1u));
+                    const float d = __fsub_rn(ys[T - 1], mul1_value(e));
+                    a.tile_cost[f_tile] = __fadd_rn(arr[ge & 8191u], __fmul_rn(d, d));
+                }
             }
         }
         if (r == 0 && tid == 0 && b_loc >= 0) {
@@ -380,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int TT>
 exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
-    const size_t smem = (size_t)(4 * 8192 + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    const size_t smem = (size_t)(3 * kBufFloats + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(encode_k1_kernel<TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
@@ -412,6 +502,22 @@ exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
 }
 
 }  // namespace
+
+exl3_status k1_take_wait_timeouts(unsigned int *n) {
+    *n = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_check(e, "device synchronise (wait timeouts)");
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    e = cudaMemcpyFromSymbol(&v, g_k1_wait_timeouts, sizeof v);
+    if (e == cudaSuccess && v != 0)
+        e = cudaMemcpyToSymbol(g_k1_wait_timeouts, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return cuda_check(e, "wait timeout count");
+    *n = v;
+    return EXL3_OK;
+}
 
 exl3_status launch_encode_k1(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     if (p.grid < 2 || (p.grid & 1))

@@ -60,7 +60,8 @@ typedef enum {
     EXL3_ERR_UNSUPPORTED = 2,  /* K outside the built set, dims not multiples of 16/128 */
     EXL3_ERR_WORKSPACE = 3,    /* ws_bytes below the minimum for this call */
     EXL3_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-    EXL3_ERR_NUMERIC = 5       /* the input has no factorisation (exl3_block_ldl) */
+    EXL3_ERR_NUMERIC = 5,      /* the input has no factorisation (exl3_block_ldl) */
+    EXL3_ERR_TIMEOUT = 6       /* a bounded device-side wait expired (exl3_wait_timeouts) */
 } exl3_status;
 
 typedef enum { EXL3_F32 = 0, EXL3_BF16 = 1 } exl3_dtype;
@@ -399,6 +400,19 @@ EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_t rows, int
 EXL3_API void exl3_profile_enable(int on);
 EXL3_API exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launches,
                               int64_t *kernel_launches);
+
+/*
+ * Device-side wait accounting (no counterpart on the pages).  At K = 1 the
+ * two blocks of an encode cluster wait on each other's pushed costs once per
+ * trellis step; each such wait gives up after one second, after which the
+ * block stops waiting for the rest of the launch and that launch's codes and
+ * costs are void.  exl3_wait_timeouts synchronises the device, stores in
+ * *count_out (may be NULL) the number of expired waits since the previous call
+ * and resets it; it returns EXL3_ERR_TIMEOUT when that number is nonzero,
+ * EXL3_ERR_CUDA when the device could not be read, else EXL3_OK.  The count is
+ * global to the process and the current device.
+ */
+EXL3_API exl3_status exl3_wait_timeouts(unsigned int *count_out);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,13 @@ def ex():
 DEV = "cuda:0"
 
 
+@pytest.fixture(autouse=True)
+def _no_expired_waits(ex):
+    """No bounded device wait (the K=1 clusters') may give up in any test."""
+    yield
+    assert ex.wait_timeouts() == 0
+
+
 def _np_codes(codes_t, K):
     return codes_t.detach().cpu().numpy().view(np.uint16).reshape(-1, 16 * K)
 
