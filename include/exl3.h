@@ -20,7 +20,8 @@
  *     (see exl3_encode_tiles for the bit layout).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
  *     is enqueued on it; no entry point synchronises the host with the device,
- *     except exl3_block_ldl, whose damping retries depend on a device result.
+ *     except exl3_block_ldl, whose damping retries depend on a device result,
+ *     and the exl3_wait_timeouts query.
  *   - The library allocates no device memory.  Scratch comes from the caller's
  *     workspace `ws` (device, 256-byte aligned) of `ws_bytes` bytes, sized with
  *     the matching *_workspace_bytes query.  The workspace must not be used by
