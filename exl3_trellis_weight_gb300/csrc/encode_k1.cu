@@ -3,15 +3,16 @@
 //
 // At K = 1 the tracked cost row has 2^15 fp32 entries (128 KiB); two copies do
 // not fit one SM's shared memory.  A tile is therefore encoded by a cluster of
-// two 1024-thread blocks on two SMs.  Unit h' (tracked entries 2h', 2h'+1)
+// two 512-thread blocks on two SMs.  Unit h' (tracked entries 2h', 2h'+1)
 // reads M(h') and M(16384 + h'); block r handles the 8192 units
-// h' = r*8192 + u2*2048 + 2*tid + m (u2 = 0..3, m = 0, 1: adjacent pairs, so
-// the two costs each array read are one 8-byte load) and keeps, in three
-// rotating buffers in its shared memory, exactly the costs its units read:
+// h' = r*8192 + u3*1024 + 2*tid + m (u3 = 0..7, m = 0, 1: adjacent pairs, so
+// the two costs each array read are one 8-byte load; 64 candidate states per
+// thread) and keeps, in three rotating buffers in its shared memory, exactly
+// the costs its units read:
 //   A[i] = M(r*8192 + i),  B[i] = M(16384 + r*8192 + i),  i in [0, 8192).
 // The writer pushes: a unit pair yields the four entries
-// g = 4 (r*4096 + u2*1024 + tid) + 0..3, read next step by block (g >> 13) & 1
-// (= u2 >> 1) as its A (r = 0) or B (r = 1) values at g & 8191 -- one 16-byte
+// g = 4 (r*4096 + u3*512 + tid) + 0..3, read next step by block (g >> 13) & 1
+// (= u3 >> 2) as its A (r = 0) or B (r = 1) values at g & 8191 -- one 16-byte
 // store, a plain shared store into the own block or an st.async into the
 // peer's that completes 16 bytes of the transaction count of the peer's
 // barrier for that buffer (no multicast).  Every read is local.
@@ -26,8 +27,9 @@
 // records it (exl3_k1_wait_timeouts).
 //
 // Everything else follows encode.cu: the same two passes, tie rules, packing,
-// 1024-word decision rows (each block writes the rows of its own entries into
-// its own workspace slice: word tid, bit 4 u2 + 2 m + j), and the same two-tile
+// decision rows (each block writes the rows of its own entries into its own
+// workspace slice: word tid of each 1024-word row, bit 4 u3 + 2 m + j; words
+// 512..1023 unused), and the same two-tile
 // pipeline with an interleaved traceback run by thread 0 of block 0; cluster
 // barriers separate the pipeline's phases.
 #include <cooperative_groups.h>
@@ -43,7 +45,13 @@ namespace {
 constexpr size_t kBlockWords = kEncodeBlockScratchBytes / sizeof(uint32_t);
 
 constexpr int kBufFloats = 16384;                    // one buffer: A[8192], B[8192]
-constexpr uint32_t kPushBytes = kThreads * 2u * 16u;  // bytes a block receives per step
+// 512 threads x 64 candidate states (256 x 128 is bit-exact too, and 9 % slower)
+constexpr int kK1Threads = 512;
+constexpr int kPairs = 4096 / kK1Threads;               // unit pairs per thread
+constexpr int kHalfPairs = kPairs / 2;                  // pairs bound for one block
+constexpr int kDecWords = kPairs / 8;                   // decision words per thread and step
+constexpr uint32_t kPushBytes = kK1Threads * kHalfPairs * 16u; // bytes a block receives per step
+static_assert(kK1Threads == 512 || kK1Threads == 256, "K=1 block size");
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // number of K=1 barrier waits that gave up (read and cleared by the host)
@@ -124,10 +132,11 @@ __device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const f
 // Where D_t(g) of tracked entry g (15 bits) lives: owner block, word, bit.
 __device__ __forceinline__ void k1_locate(uint32_t g, int &owner, int &word, int &bit) {
     const uint32_t hp = g >> 1;
-    const uint32_t i = hp & 8191u;               // u2 * 2048 + 2 tid + m
+    const uint32_t i = hp & 8191u;               // up * 2 NT + 2 tid + m
+    const uint32_t up = i / (2u * kK1Threads);
     owner = (int)(hp >> 13);
-    word = (int)((i >> 1) & 1023u);
-    bit = (int)((i >> 11) * 4u + (i & 1u) * 2u + (g & 1u));
+    word = (int)(((i >> 1) % kK1Threads) + kK1Threads * (up >> 3));
+    bit = (int)((up & 7u) * 4u + (i & 1u) * 2u + (g & 1u));
 }
 
 // traceback step helpers (thread 0 of block 0); tb.rows = slot rows in block 0's slice
@@ -151,25 +160,28 @@ __device__ __forceinline__ void k1_tb_advance(Tb &tb, uint32_t *bs) {
         tb.on = false;
 }
 
-// One step of block r: 4 unit pairs x 2 units x 2 entries x 2 candidates per
-// thread.  The squares q[u*2 + k] (unit u = 2 u2 + m, entries 2h', 2h'+1,
-// candidate k) were computed beforehand (they do not depend on the cost row).
-// A, B: this block's read buffer.  own: the array this block writes in its own
-// next buffer; peer / peer_bar: the same array in the peer's next buffer and
-// the peer's barrier for it (shared::cluster addresses).
-// FIRST: the pair processed first (2 for block 0, 0 for block 1), so the pairs
-// whose costs go to the peer block (sidx 0, 1) are computed and pushed first
-// and have the longest time to land.
+// One step of block r: kPairs unit pairs x 2 units x 2 entries x 2 candidates
+// per thread (pair up: units h' = r*8192 + up*2NT + 2 tid + m; unit u = 2 up + m;
+// the levels of candidate k of unit u are vpk[u*2 + k]).  A, B: this block's
+// read buffer.  own: the array this block writes in its own next buffer;
+// peer / peer_bar: the same array in the peer's next buffer and the peer's
+// barrier for it (shared::cluster addresses).
+// FIRST: the pair processed first (kHalfPairs for block 0, 0 for block 1), so
+// the pairs whose costs go to the peer block (sidx < kHalfPairs) are computed
+// and pushed first and have the longest time to land.
 template <bool ARGMIN, int FIRST>
 __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float *__restrict__ B,
                                         float *own, const uint32_t peer, const uint32_t peer_bar,
-                                        const unsigned long long (&q)[16], const int r,
-                                        const int tid, uint32_t &word, unsigned long long &key) {
-    word = 0u;
+                                        const uint32_t (&vpk)[4 * kPairs], const float y,
+                                        const int r, const int tid, uint32_t (&word)[kDecWords],
+                                        unsigned long long &key) {
 #pragma unroll
-    for (int sidx = 0; sidx < 4; sidx++) {
-        const int u2 = (sidx + FIRST) & 3;
-        const int i = u2 * 2048 + 2 * tid;        // units h' = r*8192 + i, i + 1
+    for (int w = 0; w < kDecWords; w++)
+        word[w] = 0u;
+#pragma unroll
+    for (int sidx = 0; sidx < kPairs; sidx++) {
+        const int up = (sidx + FIRST) % kPairs;
+        const int i = up * (2 * kK1Threads) + 2 * tid;   // units h' = r*8192 + i, i + 1
         const float2 ma = *reinterpret_cast<const float2 *>(A + i);
         const float2 mb = *reinterpret_cast<const float2 *>(B + i);
         float out[4];
@@ -177,8 +189,9 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
         for (int m = 0; m < 2; m++) {
             const float m0 = m ? ma.y : ma.x;      // M(h')
             const float m1 = m ? mb.y : mb.x;      // M(16384 + h')
-            const int u = 2 * u2 + m;
-            const unsigned long long q0 = q[u * 2 + 0], q1 = q[u * 2 + 1];
+            const int u = 2 * up + m;
+            const unsigned long long q0 = sq_pair(vpk[u * 2 + 0], y);
+            const unsigned long long q1 = sq_pair(vpk[u * 2 + 1], y);
             int best0 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 & 0xffffffffull))));
             int best1 = __float_as_int(__fadd_rn(m0, __uint_as_float((uint32_t)(q0 >> 32))));
             const int c0 = __float_as_int(__fadd_rn(m1, __uint_as_float((uint32_t)(q1 & 0xffffffffull))));
@@ -187,7 +200,8 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
             best0 = __vibmin_s32(best0, c0, &keep0);   // ties keep k = 0
             best1 = __vibmin_s32(best1, c1, &keep1);
             const uint32_t bk0 = keep0 ? 0u : 1u, bk1 = keep1 ? 0u : 1u;
-            word |= (bk0 << (4 * u2 + 2 * m)) | (bk1 << (4 * u2 + 2 * m + 1));
+            const int bit = 4 * (up & 7) + 2 * m;
+            word[up >> 3] |= (bk0 << bit) | (bk1 << (bit + 1));
             if (ARGMIN) {
                 const uint32_t g0 = 2u * (uint32_t)(r * 8192 + i + m);
                 const unsigned long long k0 =
@@ -201,11 +215,11 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
             out[2 * m + 1] = __int_as_float(best1);
         }
         if (!ARGMIN) {
-            // entries 4 (r*4096 + u2*1024 + tid) + 0..3: read next step by block u2 >> 1
-            // at array offset (u2 & 1) * 4096 + 4 tid
-            const int off = (u2 & 1) * 4096 + 4 * tid;
+            // entries 4 (r*4096 + up*NT + tid) + 0..3: read next step by block
+            // up / kHalfPairs at array offset 4 ((up % kHalfPairs) * NT + tid)
+            const int off = 4 * ((up % kHalfPairs) * kK1Threads + tid);
             const float4 v = make_float4(out[0], out[1], out[2], out[3]);
-            if (sidx < 2)
+            if (sidx < kHalfPairs)
                 push_peer(peer + 4u * (uint32_t)off, v, peer_bar);
             else
                 *reinterpret_cast<float4 *>(own + off) = v;
@@ -213,15 +227,8 @@ __device__ __forceinline__ void k1_step(const float *__restrict__ A, const float
     }
 }
 
-__device__ __forceinline__ void k1_squares(const uint32_t (&vpk)[16], const float y,
-                                           unsigned long long (&q)[16]) {
-#pragma unroll
-    for (int i = 0; i < 16; i++)
-        q[i] = sq_pair(vpk[i], y);
-}
-
 template <int TT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kK1Threads, 1)
     encode_k1_kernel(const EncodeLaunch a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
@@ -247,12 +254,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer_bar0 = cluster_addr(bar0, peer_rank);
 
     const int tid = threadIdx.x;
-    uint32_t vpk[16];
+    uint32_t vpk[4 * kPairs];
 #pragma unroll
-    for (int u = 0; u < 8; u++)
+    for (int u = 0; u < 2 * kPairs; u++)
 #pragma unroll
         for (int k = 0; k < 2; k++) {
-            const uint32_t hp = (uint32_t)(r * 8192 + (u >> 1) * 2048 + 2 * tid + (u & 1));
+            const uint32_t hp = (uint32_t)(r * 8192 + (u >> 1) * (2 * kK1Threads) + 2 * tid + (u & 1));
             const uint32_t s0 = ((uint32_t)k << 15) | (2u * hp);
             vpk[u * 2 + k] = (uint32_t)__half_as_ushort(mul1_half(s0)) |
                              ((uint32_t)__half_as_ushort(mul1_half(s0 + 1u)) << 16);
@@ -340,13 +347,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ys[tid] = __fmul_rn(__ldg(src), inv_s);
             }
             if (f_pass == 1) {
-                for (int i = tid; i < 8192; i += kThreads) {
+                for (int i = tid; i < 8192; i += kK1Threads) {
                     A0[i] = 0.0f;
                     B0[i] = 0.0f;
                 }
             } else {
                 const int ge = (int)(sh_end[f_slot] & 0x7FFFu);
-                for (int i = tid; i < 8192; i += kThreads) {
+                for (int i = tid; i < 8192; i += kK1Threads) {
                     A0[i] = (r * 8192 + i == ge) ? 0.0f : __int_as_float(0x7f800000);
                     B0[i] = (16384 + r * 8192 + i == ge) ? 0.0f : __int_as_float(0x7f800000);
                 }
@@ -379,8 +386,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t *rows = (f_pass == 1) ? scr + (size_t)f_slot * kP1
                                            : scr + 2 * kP1 + (size_t)f_slot * kP2;
             const int row0 = (f_pass == 1) ? half - 1 : 0;
-            unsigned long long q[16];
-            k1_squares(vpk, ys[0], q);
             int cur = 0;            // buffer read by step t: t mod 3
             for (int t = 0; t < T - 1; t++) {
                 const int nxt = cur == 2 ? 0 : cur + 1;
@@ -393,16 +398,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float *own = buf + nxt * kBufFloats + own_off;
                 const uint32_t peer = peer0 + (uint32_t)(nxt * kBufFloats * 4);
                 const uint32_t peer_bar = peer_bar0 + 8u * (uint32_t)nxt;
-                uint32_t word;
+                uint32_t word[kDecWords];
                 unsigned long long key = 0ull;
+                const float y = ys[t];
                 if (r == 0)
-                    k1_step<false, 2>(Ap, Ap + 8192, own, peer, peer_bar, q, r, tid, word, key);
+                    k1_step<false, kHalfPairs>(Ap, Ap + 8192, own, peer, peer_bar, vpk, y, r, tid, word, key);
                 else
-                    k1_step<false, 0>(Ap, Ap + 8192, own, peer, peer_bar, q, r, tid, word, key);
-                // work that needs no new costs: next squares, decision store, traceback
-                k1_squares(vpk, ys[t + 1], q);
-                if (t >= row0)
-                    rows[(size_t)(t - row0) * kRowWords + tid] = word;
+                    k1_step<false, 0>(Ap, Ap + 8192, own, peer, peer_bar, vpk, y, r, tid, word, key);
+                // work that needs no new costs: decision store, traceback
+                if (t >= row0) {
+#pragma unroll
+                    for (int w = 0; w < kDecWords; w++)
+                        rows[(size_t)(t - row0) * kRowWords + tid + w * kK1Threads] = word[w];
+                }
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
                 __syncthreads();                                  // own stores
@@ -411,13 +419,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cur = nxt;
             }
             if (f_pass == 1) {
-                // last step (reads M_{T-2} from buffer cur); q holds its squares
+                // last step (reads M_{T-2} from buffer cur)
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_issue(tb);
-                uint32_t word;
+                uint32_t word[kDecWords];
                 unsigned long long key = ~0ull;
                 const float *Ap = buf + cur * kBufFloats;
-                k1_step<true, 0>(Ap, Ap + 8192, nullptr, 0u, 0u, q, r, tid, word, key);
+                k1_step<true, 0>(Ap, Ap + 8192, nullptr, 0u, 0u, vpk, ys[T - 1], r, tid, word, key);
                 if (r == 0 && tid == 0 && tb.on)
                     k1_tb_advance(tb, bs);
                 key = warp_min_u64(key);
@@ -425,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     red[tid >> 5] = key;
                 __syncthreads();
                 if (tid < 32) {
-                    key = warp_min_u64(red[tid]);
+                    key = warp_min_u64(tid < kK1Threads / 32 ? red[tid] : ~0ull);
                     if (tid == 0)
                         sh_key = key;
                 }
@@ -480,7 +488,7 @@ exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     EncodeLaunch q = p;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kK1Threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     int n_clusters = 0;
@@ -493,7 +501,7 @@ exl3_status launch_k1_t(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
         q.grid = 2 * n_clusters;
     if (profiled)
         profile_encode_begin(s);
-    encode_k1_kernel<TT><<<q.grid, kThreads, smem, s>>>(q);
+    encode_k1_kernel<TT><<<q.grid, kK1Threads, smem, s>>>(q);
     if (profiled) {
         note_launch();
         profile_encode_end(s);
