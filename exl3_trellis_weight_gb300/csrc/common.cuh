@@ -71,13 +71,18 @@ __device__ __forceinline__ uint32_t window_state_k(const uint32_t *w, int i, int
 //   predecessor:   sigma_k >> K = (k << (16-2K)) | (g >> K)
 // A "unit" h' = g >> K groups the 2^K tracked entries g = (h' << K) | j that
 // read the same 2^K predecessor costs M((k << (16-2K)) | h').  Each of the
-// 1024 threads of an encode block owns 64 candidate states:
-//   K=2: 4 units x 4 groups x 4 candidates   (units h' = u*1024 + tid)
-//   K=3: 1 unit  x 8 groups x 8 candidates   (unit h' = tid)
-//   K=4: 1/4 unit: 4 groups x 16 candidates  (unit h' = tid >> 2,
-//                                             groups 4*(tid & 3) .. +3)
+// 512 threads of an encode block owns 128 candidate states:
+//   K=2: 8 units x 4 groups x 4 candidates   (units h' = u*512 + tid)
+//   K=3: 2 units x 8 groups x 8 candidates   (units h' = u*512 + tid)
+//   K=4: 1/2 unit: 8 groups x 16 candidates  (unit h' = tid >> 1,
+//                                             groups 8*(tid & 1) .. +7)
+// The K-bit decisions of a thread's entries fill UPW units per 32-bit word
+// (K=2: 4, K=3: 1, K=4: 1), DW words per thread and step (2, 2, 1).
 // ---------------------------------------------------------------------------
-constexpr int kThreads = 1024;
+// Encode block size (K >= 2): 512 threads x 128 candidate states, up to 128
+// registers each (1024 x 64 at 64 registers measured 3 % slower at K=2, 12 %
+// at K=4).
+constexpr int kThreads = 512;
 
 template <int K>
 struct Geo {
@@ -88,9 +93,11 @@ struct Geo {
     static constexpr int NU = UNITS >= kThreads ? UNITS / kThreads : 1;  // units per thread
     static constexpr int TPU = UNITS >= kThreads ? 1 : kThreads / UNITS; // threads per unit
     static constexpr int NJ = NK / TPU;                                  // groups per thread-unit
-    static constexpr int STATES = NU * NJ * NK;                          // = 64
-    static_assert(STATES == 64, "each thread owns 64 candidate states");
-    static_assert(NU * NJ * K <= 32, "decisions of one thread fit a 32-bit word");
+    static constexpr int STATES = NU * NJ * NK;                          // candidate states per thread
+    static constexpr int UPW = 32 / (NJ * K);                            // units per decision word
+    static constexpr int DW = (NU + UPW - 1) / UPW;                      // decision words per thread
+    static_assert(STATES * kThreads == 65536, "the threads own all 2^16 candidate states");
+    static_assert(UPW >= 1, "a unit's decisions fit one 32-bit word");
 
     __device__ __forceinline__ static int unit(int u, int tid) {
         return TPU == 1 ? u * kThreads + tid : (tid / TPU);
@@ -98,14 +105,20 @@ struct Geo {
     __device__ __forceinline__ static int j0(int tid) {
         return TPU == 1 ? 0 : (tid % TPU) * NJ;
     }
+    // Bit of entry j (0..NJ-1 of the thread's share) of unit u in decision word u / UPW.
+    __host__ __device__ __forceinline__ static constexpr int dec_bit(int u, int j) {
+        return ((u % UPW) * NJ + j) * K;
+    }
     // Location of D_t(g) inside a decision row: (word index, bit position).
+    // Word w of thread tid is row word tid + w * kThreads.
     __host__ __device__ __forceinline__ static void dec_locate(uint32_t g, int &word, int &bit) {
         uint32_t hp = g >> K;
         uint32_t j = g & (NK - 1);
         if (TPU == 1) {
-            word = (int)(hp & (kThreads - 1));
-            int u = (int)(hp / kThreads);
-            bit = (u * NJ + (int)j) * K;
+            const int tid = (int)(hp % kThreads);
+            const int u = (int)(hp / kThreads);
+            word = tid + kThreads * (u / UPW);
+            bit = dec_bit(u, (int)j);
         } else {
             word = (int)(hp * TPU + j / NJ);
             bit = (int)(j % NJ) * K;
@@ -113,8 +126,9 @@ struct Geo {
     }
 };
 
-// Decision rows: one 32-bit word per thread per step (4 KiB per row).
-constexpr int kRowWords = kThreads;
+// Decision rows: 1024 32-bit words per step (4 KiB per row); an encode thread
+// writes words tid + w * kThreads, w < Geo<K>::DW.
+constexpr int kRowWords = 1024;
 constexpr int kRowsPass1 = 128;   // steps 127..254 of the rolled pass
 constexpr int kRowsPass2 = 255;   // steps 0..254 of the constrained pass
 constexpr size_t kEncodeBlockScratchBytes =

@@ -1,7 +1,7 @@
 // encode.cu -- persistent trellis tile encoder (page "EXL3 Intel Arc
 // Quantizer", Core Implemented Architecture items 1, 4 and 5).
 //
-// One 1024-thread block per SM walks its share of the tiles.  A tile is T
+// One 512-thread block per SM walks its share of the tiles.  A tile is T
 // targets: the 256 elements of a 16x16 tile (row-major), or one row of T
 // elements (even T in [16, 256]).  For each tile:
 //   pass 1: targets rolled left by T/2, free start, T add-compare-select
@@ -13,10 +13,10 @@
 //           low K bits of each state are packed MSB first.
 //
 // The tracked cost row M (2^(16-K) fp32) is double-buffered in shared memory;
-// the mul1 level of each of a thread's 64 candidate states is fixed for the
+// the mul1 level of each of a thread's 128 candidate states is fixed for the
 // whole launch and is kept in registers as packed fp16.  Decisions (K bits per
-// tracked entry per step, one 32-bit word per thread per step) go to the
-// block's slice of the workspace.
+// tracked entry per step, one or two 32-bit words per thread per step) go to
+// the block's slice of the workspace.
 //
 // The traceback is a chain of dependent loads, so it is overlapped with the
 // forward pass of another tile: the block keeps two tiles A and B in flight
@@ -34,10 +34,13 @@ namespace {
 #endif
 template <int K, bool ARGMIN>
 __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__restrict__ Mn,
-                                         const float y, const uint32_t (&vpk)[32], const int tid,
-                                         uint32_t &word, unsigned long long &key) {
+                                         const float y, const uint32_t (&vpk)[Geo<K>::STATES / 2],
+                                         const int tid, uint32_t (&word)[Geo<K>::DW],
+                                         unsigned long long &key) {
     using Gm = Geo<K>;
-    word = 0u;
+#pragma unroll
+    for (int w = 0; w < Gm::DW; w++)
+        word[w] = 0u;
 #pragma unroll
     for (int u = 0; u < Gm::NU; u++) {
         const int hp = Gm::unit(u, tid);
@@ -141,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     const int tid = threadIdx.x;
 
     // mul1 levels of this thread's candidate states, packed two per register
-    uint32_t vpk[32];
+    uint32_t vpk[Gm::STATES / 2];
 #pragma unroll
     for (int u = 0; u < Gm::NU; u++)
 #pragma unroll
@@ -260,11 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                     tb_issue<K>(tb);
                 const float *Mp = (t & 1) ? M1 : M0;
                 float *Mn = (t & 1) ? M0 : M1;
-                uint32_t word;
+                uint32_t word[Gm::DW];
                 unsigned long long key = 0ull;
                 acs_step<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
-                if (t >= row0)
-                    rows[(size_t)(t - row0) * kRowWords + tid] = word;
+                if (t >= row0) {
+#pragma unroll
+                    for (int w = 0; w < Gm::DW; w++)
+                        rows[(size_t)(t - row0) * kRowWords + tid + w * kThreads] = word[w];
+                }
                 if (tid == 0 && tb.on)
                     tb_advance<K>(tb, bs);
                 __syncthreads();
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 // step T-1 (T even: reads M_{T-2} from M1): lowest full state with minimal cost
                 if (tid == 0 && tb.on)
                     tb_issue<K>(tb);
-                uint32_t word;
+                uint32_t word[Gm::DW];
                 unsigned long long key = ~0ull;
                 acs_step<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
                 if (tid == 0 && tb.on)
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                     red[tid >> 5] = key;
                 __syncthreads();
                 if (tid < 32) {
-                    key = warp_min_u64(red[tid]);
+                    key = warp_min_u64(tid < kThreads / 32 ? red[tid] : ~0ull);
                     if (tid == 0)
                         sh_sstar[f_slot] = (uint32_t)(key & 0xffffffffull);
                 }

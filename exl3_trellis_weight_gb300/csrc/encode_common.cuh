@@ -101,12 +101,13 @@ __device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, cons
 template <int K, bool ARGMIN>
 __device__ __forceinline__ void finish_pair(const int u, const int jp, const int hp, const int j0,
                                             const int best0, const int best1, const uint32_t bk0,
-                                            const uint32_t bk1, float *outv, uint32_t &word,
+                                            const uint32_t bk1, float *outv,
+                                            uint32_t (&word)[Geo<K>::DW],
                                             unsigned long long &key) {
     using Gm = Geo<K>;
     outv[jp] = __int_as_float(best0);
     outv[jp + 1] = __int_as_float(best1);
-    word |= (bk0 << ((u * Gm::NJ + jp) * K)) | (bk1 << ((u * Gm::NJ + jp + 1) * K));
+    word[u / Gm::UPW] |= (bk0 << Gm::dec_bit(u, jp)) | (bk1 << Gm::dec_bit(u, jp + 1));
     if (ARGMIN) {
         const uint32_t g0 = ((uint32_t)hp << K) | (uint32_t)(j0 + jp);
         const unsigned long long k0 =
