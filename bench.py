@@ -47,10 +47,11 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # DRAM traffic of one encode launch per tile, from an ncu capture; valid only
 # for the source it was taken on.
 ENCODE_TRAFFIC = {
-    # sha256 of csrc/encode.cu -> DRAM bytes (read + write) per tile at K=2, from
-    # `ncu --set full` on 1,216 tiles of N(0, 1) targets (profile case `encode`); the
-    # traffic is the decision rows, proportional to the tiles processed.
-    "36bba21314bc4c80f2b5ddd9e4436322fd4c311bbc344bac8df95c1dbc57f75d": 1545546.0,
+    # sha256 of csrc/encode.cu + encode_common.cuh + common.cuh -> DRAM bytes (read +
+    # write) per tile at K=2, from `ncu --set full` on 1,216 tiles of N(0, 1) targets
+    # (profile case `encode`); the traffic is the decision rows, proportional to the
+    # tiles processed.
+    "130ef0b185f7fa028110f502d136a4979f252a52f13f50026af32b09d425a528": 1545839.0,
 }
 
 WORKLOAD = "linear4096_k2"
@@ -67,9 +68,16 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
 
 
-def _src_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def _src_sha(*paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+ENCODE_SOURCES = [os.path.join(ROOT, "exl3_trellis_weight_gb300", "csrc", n)
+                  for n in ("encode.cu", "encode_common.cuh", "common.cuh")]
 
 
 class ClockSampler:
@@ -282,7 +290,7 @@ def run_ours(args):
     enc_launch_s = (enc_ms / max(enc_n, 1)) / 1e3
     ops_launch = alg_ops_per_tile(K) * n_tiles
     achieved = ops_launch / enc_launch_s / 1e12
-    sha = _src_sha(os.path.join(ROOT, "exl3_trellis_weight_gb300", "csrc", "encode.cu"))
+    sha = _src_sha(*ENCODE_SOURCES)
     tpt = ENCODE_TRAFFIC.get(sha)
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Tops/s",
                 "frac": achieved / peak_tops,

@@ -30,60 +30,39 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
     return v;
 }
 
-// fl(v - y) with v an fp16 value held in 16 bits (one mixed-precision subtract;
-// exact widening of v, one binary32 rounding).  (v - y)^2 == (y - v)^2 bitwise.
-__device__ __forceinline__ float sub_h_f(unsigned short v, float y) {
-    float r;
-    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(v), "f"(y));
-    return r;
-}
-
-// Two independent binary32 multiplies in one instruction.
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
-    unsigned long long r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
-    return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair:
+// the two mixed-precision subtracts (exact widening of v, one binary32
+// rounding; (v - y)^2 == (y - v)^2 bitwise) write the halves of the 64-bit
+// operand of one f32x2 multiply (one asm block, no register shuffling).
+__device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const float y) {
+    unsigned long long q;
+    asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
+        "mov.b32 {hl, hh}, %1;\n\t"
+        "sub.rn.f32.f16 a, hl, %2;\n\t"
+        "sub.rn.f32.f16 b, hh, %2;\n\t"
+        "mov.b64 d, {a, b};\n\t"
+        "mul.rn.f32x2 %0, d, d;\n\t}"
+        : "=l"(q) : "r"(vw), "f"(y));
+    return q;
 }
 
 // Candidate k of a pair of tracked entries (jj, jj+1) sharing predecessor cost
-// mk: c = fl(mk + fl(fl(v - y)^2)) for both.  The square of the pair runs as one
-// f32x2 multiply; the add stays scalar, because the compiler contracts a packed
-// multiply feeding a packed add into a fused multiply-add whatever the rounding
-// qualifiers, and a fused result differs from the two-rounding definition.
-// With FUSED_ASM the two mixed-precision subtracts write the halves of the
-// multiply's 64-bit operand directly (one asm block, no register shuffling);
-// that form is faster at K=2 and costs registers at K=3 and K=4.
-template <bool FUSED_ASM>
+// mk: c = fl(mk + fl(fl(v - y)^2)) for both.  The add stays scalar, because the
+// compiler contracts a packed multiply feeding a packed add into a fused
+// multiply-add whatever the rounding qualifiers, and a fused result differs
+// from the two-rounding definition.
 __device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, const float y,
                                           int &c0, int &c1) {
-    unsigned long long q;
-    if constexpr (FUSED_ASM) {
-        asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
-            "mov.b32 {hl, hh}, %1;\n\t"
-            "sub.rn.f32.f16 a, hl, %2;\n\t"
-            "sub.rn.f32.f16 b, hh, %2;\n\t"
-            "mov.b64 d, {a, b};\n\t"
-            "mul.rn.f32x2 %0, d, d;\n\t}"
-            : "=l"(q) : "r"(vw), "f"(y));
-    } else {
-        const float d0 = sub_h_f((unsigned short)(vw & 0xFFFFu), y);
-        const float d1 = sub_h_f((unsigned short)(vw >> 16), y);
-        const unsigned long long dd = pack2(d0, d1);
-        q = mul2(dd, dd);
-    }
+    const unsigned long long q = sq_pair(vw, y);
     c0 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q & 0xffffffffull))));
     c1 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q >> 32))));
 }
 
 // Candidate k of the pair, then the running minimum (ties keep the lower k).
-template <bool FUSED_ASM>
 __device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
                                          int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
     int c0, c1;
-    cand_pair<FUSED_ASM>(mk, vw, y, c0, c1);
+    cand_pair(mk, vw, y, c0, c1);
     if (k == 0) {
         best0 = c0;
         best1 = c1;

@@ -115,20 +115,6 @@ __device__ __forceinline__ void bar_wait(uint32_t a, uint32_t parity, volatile i
         bar_wait_slow(a, parity, gave_up);
 }
 
-// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair
-// (same operations as cand_pair<true>, without the add)
-__device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const float y) {
-    unsigned long long q;
-    asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
-        "mov.b32 {hl, hh}, %1;\n\t"
-        "sub.rn.f32.f16 a, hl, %2;\n\t"
-        "sub.rn.f32.f16 b, hh, %2;\n\t"
-        "mov.b64 d, {a, b};\n\t"
-        "mul.rn.f32x2 %0, d, d;\n\t}"
-        : "=l"(q) : "r"(vw), "f"(y));
-    return q;
-}
-
 // Where D_t(g) of tracked entry g (15 bits) lives: owner block, word, bit.
 __device__ __forceinline__ void k1_locate(uint32_t g, int &owner, int &word, int &bit) {
     const uint32_t hp = g >> 1;
