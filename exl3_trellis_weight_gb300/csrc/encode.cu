@@ -29,12 +29,15 @@
 namespace exl3 {
 
 namespace {
-// One add-compare-select step of a thread's units.  For each unit the NK
-// predecessor costs are loaded once and kept in registers; the entries are
-// taken a pair at a time (one packed square per candidate pair).  The other
-// orders tried -- reloading the predecessor cost for every pair, or keeping
-// the running minima of all entries live and streaming the costs -- ran at
-// the same speed (K=3, K=4) or up to 77 % slower (K=4, running minima).
+// One add-compare-select step of a thread's units.  The NK predecessor costs of
+// a unit are loaded once and each is duplicated into both halves of a 64-bit
+// register pair; the entries are taken a pair at a time, so every candidate
+// pair is one packed square (an FMA with a +0 addend) and one packed add.
+// Measured against the alternatives at 512 threads: scalar adds 4-6 % slower
+// (K=2..4); pairing the same (k, j) of two units instead of two entries of one
+// unit (the two costs then load straight into a pair) 1-9 % slower; reloading
+// the cost for every entry pair the same speed; keeping all running minima
+// live while the costs stream 6 % slower at K=2 and 77 % at K=4.
 template <int K, bool ARGMIN>
 __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__restrict__ Mn,
                                          const float y, const uint32_t (&vpk)[Geo<K>::STATES / 2],
@@ -49,18 +52,19 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
         const int hp = Gm::unit(u, tid);
         const int j0 = Gm::j0(tid);
         float outv[Gm::NJ];
-        float m[Gm::NK];
+        unsigned long long mm[Gm::NK];
 #pragma unroll
-        for (int k = 0; k < Gm::NK; k++)
-            m[k] = Mp[(k << (16 - 2 * K)) + hp];
+        for (int k = 0; k < Gm::NK; k++) {
+            const float m = Mp[(k << (16 - 2 * K)) + hp];
+            mm[k] = pack_costs(m, m);
+        }
 #pragma unroll
         for (int jp = 0; jp < Gm::NJ; jp += 2) {
             int best0 = 0, best1 = 0;
             uint32_t bk0 = 0u, bk1 = 0u;
 #pragma unroll
             for (int k = 0; k < Gm::NK; k++)
-                acs_pair(m[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1, bk0,
-                         bk1);
+                acs2(mm[k], vpk[((u * Gm::NK + k) * Gm::NJ + jp) >> 1], y, k, best0, best1, bk0, bk1);
             finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
         }
         if (!ARGMIN) {

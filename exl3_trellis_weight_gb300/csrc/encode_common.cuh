@@ -30,10 +30,11 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
     return v;
 }
 
-// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair:
-// the two mixed-precision subtracts (exact widening of v, one binary32
-// rounding; (v - y)^2 == (y - v)^2 bitwise) write the halves of the 64-bit
-// operand of one f32x2 multiply (one asm block, no register shuffling).
+// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair: the
+// two mixed-precision subtracts (exact widening of v, one binary32 rounding;
+// (v - y)^2 == (y - v)^2 bitwise) write the halves of the 64-bit operand of one
+// f32x2 multiply.  The K=1 encoder adds the costs with scalar adds (the packed
+// form below measured 0.8 % slower there).
 __device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const float y) {
     unsigned long long q;
     asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
@@ -46,23 +47,41 @@ __device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const f
     return q;
 }
 
-// Candidate k of a pair of tracked entries (jj, jj+1) sharing predecessor cost
-// mk: c = fl(mk + fl(fl(v - y)^2)) for both.  The add stays scalar, because the
-// compiler contracts a packed multiply feeding a packed add into a fused
-// multiply-add whatever the rounding qualifiers, and a fused result differs
-// from the two-rounding definition.
-__device__ __forceinline__ void cand_pair(const float mk, const uint32_t vw, const float y,
-                                          int &c0, int &c1) {
-    const unsigned long long q = sq_pair(vw, y);
-    c0 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q & 0xffffffffull))));
-    c1 = __float_as_int(__fadd_rn(mk, __uint_as_float((uint32_t)(q >> 32))));
+// Two candidates: fl(m + fl(fl(v - y)^2)) for the two fp16 levels packed in vw
+// and the two predecessor costs packed in mm, as one 64-bit pair.  The two
+// mixed-precision subtracts (exact widening of v, one binary32 rounding) write
+// the halves of a 64-bit operand; the square is a packed FMA with a +0 addend --
+// exactly fl(d*d), since d*d is never -0 -- and the add is packed too.  A plain
+// packed multiply would not do: the compiler contracts a packed multiply feeding
+// a packed add into a fused multiply-add whatever the rounding qualifiers, and a
+// fused result differs from the two-rounding definition (measured: 3.4 % of
+// random candidates; none with the FMA form).
+__device__ __forceinline__ unsigned long long cand2(const uint32_t vw, const float y,
+                                                    const unsigned long long mm) {
+    unsigned long long c;
+    asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d, q, z;\n\t"
+        "mov.b32 {hl, hh}, %1;\n\t"
+        "sub.rn.f32.f16 a, hl, %2;\n\t"
+        "sub.rn.f32.f16 b, hh, %2;\n\t"
+        "mov.b64 d, {a, b};\n\t"
+        "mov.b64 z, 0;\n\t"
+        "fma.rn.f32x2 q, d, d, z;\n\t"
+        "add.rn.f32x2 %0, %3, q;\n\t}"
+        : "=l"(c) : "r"(vw), "f"(y), "l"(mm));
+    return c;
 }
 
-// Candidate k of the pair, then the running minimum (ties keep the lower k).
-__device__ __forceinline__ void acs_pair(const float mk, const uint32_t vw, const float y, const int k,
-                                         int &best0, int &best1, uint32_t &bk0, uint32_t &bk1) {
-    int c0, c1;
-    cand_pair(mk, vw, y, c0, c1);
+__device__ __forceinline__ unsigned long long pack_costs(const float lo, const float hi) {
+    return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+
+// Candidate k of two entries (predecessor costs packed in mm), then the running
+// minima (ties keep the lower k).
+__device__ __forceinline__ void acs2(const unsigned long long mm, const uint32_t vw, const float y,
+                                     const int k, int &best0, int &best1, uint32_t &bk0,
+                                     uint32_t &bk1) {
+    const unsigned long long c = cand2(vw, y, mm);
+    const int c0 = (int)(uint32_t)(c & 0xffffffffull), c1 = (int)(uint32_t)(c >> 32);
     if (k == 0) {
         best0 = c0;
         best1 = c1;
