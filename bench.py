@@ -51,7 +51,7 @@ ENCODE_TRAFFIC = {
     # write) per tile at K=2, from `ncu --set full` on 1,216 tiles of N(0, 1) targets
     # (profile case `encode`); the traffic is the decision rows, proportional to the
     # tiles processed.
-    "130ef0b185f7fa028110f502d136a4979f252a52f13f50026af32b09d425a528": 1545839.0,
+    "a0edf80318fa56e3c1274a1b04655209b9c106594b6098ea592ddc1f2f2732d1": 1546270.0,
 }
 
 WORKLOAD = "linear4096_k2"
