@@ -66,6 +66,13 @@ __global__ void __launch_bounds__(1024, 1) kern(const int *in, unsigned *out, un
             if (KIND == 7) { const bool p = f[i] < fo[i]; b[i] = p ? b[i] : (unsigned)i; f[i] = __fadd_rn(f[i], fo[i ^ 1]); } // compare + select + fadd
             if (KIND == 8) b[i] = b[i] * (unsigned)op[i] + (unsigned)op[i ^ 1];
             if (KIND == 10) b[i] = __byte_perm(b[i], (unsigned)op[i], 0x5410);
+            if (KIND == 11) f[i] = fminf(fminf(__fadd_rn(f[i], fo[i]), fo[i ^ 1]), fo[i ^ 2]);  // fadd + 2 fmnmx
+            if (KIND == 15) {                                                             // fadd + fsetp + fmnmx + sel
+                const float v = __fadd_rn(f[i], fo[i]);
+                const bool p = v < fo[i ^ 1];
+                f[i] = fminf(v, fo[i ^ 1]);
+                b[i] = p ? (unsigned)i : b[i];
+            }
         }
     }
     unsigned acc = 0;
@@ -124,6 +131,11 @@ int main() {
     run<7>("fp32 compare + select + fp32 add", 3, sms, din, dout, dcyc);
     run<8>("integer multiply-add", 1, sms, din, dout, dcyc);
     run<10>("byte permute", 1, sms, din, dout, dcyc);
+    // fp32 min: 42.7 bodies/clk if it issues to the FMA pipe (3 FMA-pipe instructions),
+    // 32 if to the 64-lane ALU pipe (2 ALU slots)
+    run<11>("fp32 add + 2 fp32 min", 3, sms, din, dout, dcyc);
+    // 32 bodies/clk if fp32 min is on the FMA pipe (compare + select = 2 ALU slots), 21.3 if on the ALU
+    run<15>("fp32 add + compare + min + select", 4, sms, din, dout, dcyc);
     cudaFree(din);
     cudaFree(dout);
     cudaFree(dcyc);
