@@ -15,7 +15,7 @@ import math
 import numpy as np
 
 
-def golden_section_search(f, lo: float, hi: float, n_eval: int):
+def golden_section_search(f, lo: float, hi: float, n_eval: int, return_bracket: bool = False):
     """Minimise f over [lo, hi] with exactly ``n_eval`` (>= 2) evaluations.
 
     phi = (sqrt(5) - 1) / 2.  Start with x1 = b - phi (b - a), x2 = a + phi (b - a)
@@ -23,7 +23,8 @@ def golden_section_search(f, lo: float, hi: float, n_eval: int):
     [a, x2]: b <- x2, x2 <- x1, x1 <- b - phi (b - a), evaluate x1; otherwise it
     lies in [x1, b]: a <- x1, x1 <- x2, x2 <- a + phi (b - a), evaluate x2.
     Returns (best_x, best_f, history) where best is the evaluated point with the
-    least f, the smaller x on ties, and history lists (x, f) in evaluation order.
+    least f, the smaller x on ties, and history lists (x, f) in evaluation order;
+    with ``return_bracket`` also the final bracket (a, b).
     """
     if n_eval < 2:
         raise ValueError("golden-section search needs at least two evaluations")
@@ -53,6 +54,8 @@ def golden_section_search(f, lo: float, hi: float, n_eval: int):
     for x, fx in hist[1:]:
         if fx < best_f or (fx == best_f and x < best_x):
             best_x, best_f = x, fx
+    if return_bracket:
+        return best_x, best_f, hist, (a, b)
     return best_x, best_f, hist
 
 
