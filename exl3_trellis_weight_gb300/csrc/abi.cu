@@ -965,8 +965,11 @@ exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launches, int64
 }  // extern "C"
 
 exl3_status exl3_wait_timeouts(unsigned int *count_out) {
-    unsigned int n = 0;
-    const exl3_status st = exl3::k1_take_wait_timeouts(&n);
+    unsigned int n = 0, r = 0;
+    exl3_status st = exl3::k1_take_wait_timeouts(&n);   // synchronises the device
+    if (st == EXL3_OK)
+        st = exl3::rot_take_wait_timeouts(&r);
+    n += r;
     if (count_out)
         *count_out = n;
     if (st != EXL3_OK)

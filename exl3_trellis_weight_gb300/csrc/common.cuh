@@ -195,6 +195,12 @@ exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s);
 // 16-byte aligned in / sv / out; launch_rotate picks it when eligible
 bool rotate_fwd_eligible(const RotateLaunch &p);
 exl3_status launch_rotate_fwd(const RotateLaunch &p, cudaStream_t s);
+// the same with TMA staging (rotate_fwd_tma.cu): bf16 source, fp32 output, 16-byte
+// aligned; EXL3_ERR_UNSUPPORTED when no tensor map can be encoded for the pointers
+bool rotate_fwd_tma_eligible(const RotateLaunch &p);
+exl3_status launch_rotate_fwd_tma(const RotateLaunch &p, cudaStream_t s);
+// reads and clears the TMA rotation's expired-wait count (no synchronisation)
+exl3_status rot_take_wait_timeouts(unsigned int *n);
 
 // grid-and-parabola scale search (scale_search.cu)
 struct GridSearchLaunch {

@@ -193,6 +193,11 @@ exl3_status launch_rotate_fwd(const RotateLaunch &p, cudaStream_t s) {
     const int64_t nblk = (p.rows / 128) * (p.cols / 128);
     if (nblk == 0)
         return EXL3_OK;
+    if (rotate_fwd_tma_eligible(p)) {
+        const exl3_status st = launch_rotate_fwd_tma(p, s);
+        if (st != EXL3_ERR_UNSUPPORTED)
+            return st;
+    }
     const size_t smem = (size_t)128 * 128 * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rotate_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

@@ -1,0 +1,369 @@
+// rotate_fwd_tma.cu -- forward blockwise Sylvester Hadamard rotation of a bf16
+// matrix with TMA staging (page "EXL3 Intel Arc Quantizer", Core Implemented
+// Architecture item 7: R = H (su . W . sv) H per 128 x 128 block, unnormalised
+// butterflies then one exact 2^-7).
+//
+// Same arithmetic and stage order as rotate_fwd.cu (bit-identical results);
+// what differs is the data movement.  One persistent 512-thread block per SM
+// walks the 128 x 128 blocks blockIdx.x, + gridDim.x, ...:
+//   - the bf16 block arrives by two TMA loads (64-column boxes, 128-byte
+//     swizzle) into one of two input stages, with its 128 column signs sv and
+//     128 row signs su (two 512-byte bulk copies on the same transaction
+//     barrier); the loads of the next block are issued before the current one
+//     is transformed, so they overlap the work;
+//   - the fp32 result is written to an output stage in shared memory and
+//     leaves by one TMA store (128 x 128 box) that overlaps the next block;
+//   - between the three butterfly phases the block is exchanged through a
+//     transpose buffer whose 16-byte groups are XOR-swizzled by the row
+//     (offset function tr_off), so every phase's shared accesses are
+//     conflict-free.
+// Phase 1 takes 8 rows per group of 8 lanes (lane bits 0-2 = row, 3-4 = column
+// quarter), so its 16-byte reads of the swizzled input stage hit 8 distinct
+// bank groups.  Shared memory: 2 x 33 KiB input stages, 64 KiB transpose
+// buffer, 64 KiB output stage.
+//
+// Each wait for a TMA load is bounded in time: on expiry the block stops
+// waiting, its results are void, and a device counter records it (read with
+// the K=1 encoder's count by exl3_wait_timeouts).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kTmaThreads = 512;
+constexpr uint32_t kBlockBytes = 128 * 128 * 2;        // one bf16 block (two 16 KiB boxes)
+constexpr uint32_t kSignBytes = 2 * 128 * 4;           // sv[c0 .. c0+127], su[r0 .. r0+127]
+constexpr uint32_t kStageBytes = kBlockBytes + 1024;   // keeps every stage 1024-byte aligned
+constexpr uint32_t kTOff = 2 * kStageBytes;            // transpose buffer
+constexpr uint32_t kOOff = kTOff + 128 * 128 * 4;      // output stage
+constexpr uint32_t kSmemBytes = kOOff + 128 * 128 * 4; // 194 KiB
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ unsigned int g_rot_wait_timeouts;
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// transpose buffer: row i (128 floats), 16-byte group g = j >> 2 stored at g ^ (i & 7)
+__device__ __forceinline__ int tr_off(int i, int j) {
+    return i * 128 + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3);
+}
+
+template <int SPAN, int N>
+__device__ __forceinline__ void bfly(float (&x)[N]) {
+#pragma unroll
+    for (int e = 0; e < N; e++) {
+        if ((e & SPAN) == 0) {
+            const float a = x[e], b = x[e + SPAN];
+            x[e] = __fadd_rn(a, b);
+            x[e + SPAN] = __fsub_rn(a, b);
+        }
+    }
+}
+
+__device__ __forceinline__ bool bar_test(uint32_t a, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    return ok != 0u;
+}
+
+__device__ __noinline__ void bar_wait_slow(uint32_t a, uint32_t parity, volatile int *gave_up) {
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
+    while (!bar_test(a, parity)) {
+        if (*gave_up)
+            return;
+        unsigned long long t1;
+        asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
+        if (t1 - t0 > kWaitLimitNs) {
+            *gave_up = 1;
+            atomicAdd(&g_rot_wait_timeouts, 1u);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void bar_wait(uint32_t a, uint32_t parity, volatile int *gave_up) {
+    if (!bar_test(a, parity))
+        bar_wait_slow(a, parity, gave_up);
+}
+
+// thread 0: both 64-column boxes of block blk and its sign slices into input
+// stage `stage` (block at +0, sv at +kBlockBytes, su at +kBlockBytes + 512)
+__device__ __forceinline__ void issue_load(const CUtensorMap *map, const float *su, const float *sv,
+                                           uint32_t stage_addr, uint32_t bar, int blk, int nbc) {
+    const int r0 = (blk / nbc) * 128, c0 = (blk % nbc) * 128;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(kBlockBytes + kSignBytes) : "memory");
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+        asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+                     "[%0], [%1, {%2, %3}], [%4];"
+                     :: "r"(stage_addr + (uint32_t)h * (kBlockBytes / 2)), "l"((uint64_t)map),
+                        "r"(c0 + 64 * h), "r"(r0), "r"(bar)
+                     : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 512, [%2];"
+                 :: "r"(stage_addr + kBlockBytes), "l"((uint64_t)(sv + c0)), "r"(bar) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 512, [%2];"
+                 :: "r"(stage_addr + kBlockBytes + 512u), "l"((uint64_t)(su + r0)), "r"(bar) : "memory");
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    rotate_fwd_tma_kernel(const __grid_constant__ CUtensorMap in_map,
+                          const __grid_constant__ CUtensorMap out_map, const float *__restrict__ su,
+                          const float *__restrict__ sv, const int rows, const int cols,
+                          double *tile_sums) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) unsigned long long full[2];
+    __shared__ int gave_up;
+    // the swizzled TMA destinations want 1024-byte alignment
+    const uint32_t raw = saddr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *const sb = smem_raw + (base - raw);
+    float *const T = reinterpret_cast<float *>(sb + kTOff);
+    float *const O = reinterpret_cast<float *>(sb + kOOff);
+    const int t = threadIdx.x;
+    const int nbc = cols / 128;
+    const int nblk = (rows / 128) * nbc;
+    const uint32_t bar0 = saddr(&full[0]);
+
+    if (t == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0 + 8u) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        gave_up = 0;
+    }
+    __syncthreads();
+    if (t == 0 && (int)blockIdx.x < nblk)
+        issue_load(&in_map, su, sv, base, bar0, (int)blockIdx.x, nbc);
+
+    int it = 0;
+    for (int blk = (int)blockIdx.x; blk < nblk; blk += (int)gridDim.x, it++) {
+        const int st = it & 1;
+        const int r0 = (blk / nbc) * 128, c0 = (blk % nbc) * 128;
+        // the other stage was last read in the previous block's phase 1
+        if (t == 0 && blk + (int)gridDim.x < nblk)
+            issue_load(&in_map, su, sv, base + (uint32_t)(st ^ 1) * kStageBytes,
+                       bar0 + 8u * (uint32_t)(st ^ 1), blk + (int)gridDim.x, nbc);
+        bar_wait(bar0 + 8u * (uint32_t)st, (uint32_t)(it >> 1) & 1u, &gave_up);
+
+        // ---- phase 1: row i, columns 32 jh .. 32 jh + 31 -> j spans 1..16 -------
+        {
+            const int i = (t & 7) + 8 * (t >> 5), jh = (t >> 3) & 3;
+            const unsigned char *stage = sb + (uint32_t)st * kStageBytes;
+            const unsigned char *row = stage + (jh >> 1) * (kBlockBytes / 2) + i * 128;
+            const float4 *svp = reinterpret_cast<const float4 *>(stage + kBlockBytes) + 8 * jh;
+            float x[32];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                // 16-byte group (jh & 1) * 4 + q of the 128-byte box row, swizzled by the row
+                const int g = ((jh & 1) * 4 + q) ^ (i & 7);
+                const uint4 w = *reinterpret_cast<const uint4 *>(row + 16 * g);
+                const float4 s0 = svp[2 * q], s1 = svp[2 * q + 1];
+                x[8 * q + 0] = __fmul_rn(__uint_as_float(w.x << 16), s0.x);
+                x[8 * q + 1] = __fmul_rn(__uint_as_float(w.x & 0xFFFF0000u), s0.y);
+                x[8 * q + 2] = __fmul_rn(__uint_as_float(w.y << 16), s0.z);
+                x[8 * q + 3] = __fmul_rn(__uint_as_float(w.y & 0xFFFF0000u), s0.w);
+                x[8 * q + 4] = __fmul_rn(__uint_as_float(w.z << 16), s1.x);
+                x[8 * q + 5] = __fmul_rn(__uint_as_float(w.z & 0xFFFF0000u), s1.y);
+                x[8 * q + 6] = __fmul_rn(__uint_as_float(w.w << 16), s1.z);
+                x[8 * q + 7] = __fmul_rn(__uint_as_float(w.w & 0xFFFF0000u), s1.w);
+            }
+            bfly<1>(x);
+            bfly<2>(x);
+            bfly<4>(x);
+            bfly<8>(x);
+            bfly<16>(x);
+#pragma unroll
+            for (int q = 0; q < 8; q++)
+                *reinterpret_cast<float4 *>(T + tr_off(i, 32 * jh + 4 * q)) =
+                    make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
+        __syncthreads();
+
+        // ---- phase 2: rows 8 ib .. 8 ib + 7, columns jlo + 32 jh ----------------
+        {
+            const int ib = t >> 5, jlo = t & 31;
+            const float *sus = reinterpret_cast<const float *>(sb + (uint32_t)st * kStageBytes + kBlockBytes + 512u);
+            float x[32];                               // x[8 jh + il]
+#pragma unroll
+            for (int jh = 0; jh < 4; jh++)
+#pragma unroll
+                for (int il = 0; il < 8; il++)
+                    x[8 * jh + il] = T[tr_off(8 * ib + il, jlo + 32 * jh)];
+            bfly<8>(x);                                // j span 32
+            bfly<16>(x);                               // j span 64
+#pragma unroll
+            for (int il = 0; il < 8; il++) {
+                const float s = sus[8 * ib + il];
+#pragma unroll
+                for (int jh = 0; jh < 4; jh++)
+                    x[8 * jh + il] = __fmul_rn(x[8 * jh + il], s);
+            }
+            bfly<1>(x);                                // i span 1
+            bfly<2>(x);                                // i span 2
+            bfly<4>(x);                                // i span 4
+#pragma unroll
+            for (int jh = 0; jh < 4; jh++)
+#pragma unroll
+                for (int il = 0; il < 8; il++)
+                    T[tr_off(8 * ib + il, jlo + 32 * jh)] = x[8 * jh + il];
+        }
+        // the previous block's store must have finished reading the output stage
+        if (t == 0)
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncthreads();
+
+        // ---- phase 3: rows ilo + 8 ih, columns 2 jp, 2 jp + 1 -> i spans 8..64 ---
+        {
+            const int ilo = t >> 6, jp = t & 63;
+            float x[32];                               // x[2 ih + jb]
+#pragma unroll
+            for (int ih = 0; ih < 16; ih++) {
+                const float2 v = *reinterpret_cast<const float2 *>(T + tr_off(ilo + 8 * ih, 2 * jp));
+                x[2 * ih] = v.x;
+                x[2 * ih + 1] = v.y;
+            }
+            bfly<2>(x);                                // i span 8
+            bfly<4>(x);                                // i span 16
+            bfly<8>(x);                                // i span 32
+            bfly<16>(x);                               // i span 64
+#pragma unroll
+            for (int ih = 0; ih < 16; ih++)
+                *reinterpret_cast<float2 *>(O + (ilo + 8 * ih) * 128 + 2 * jp) =
+                    make_float2(__fmul_rn(x[2 * ih], 0x1p-7f), __fmul_rn(x[2 * ih + 1], 0x1p-7f));
+        }
+        // generic-proxy writes of the output stage, then one TMA store of it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (t == 0) {
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                         :: "l"((uint64_t)&out_map), "r"(c0), "r"(r0), "r"(base + kOOff)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        if (tile_sums && t < 64) {
+            // per-tile fp64 sums of R^2, sequential in row-major order inside each 16x16 tile
+            const int ti = t >> 3, tj = t & 7;
+            double s = 0.0;
+            for (int i = 0; i < 16; i++)
+                for (int j = 0; j < 16; j++) {
+                    const double v = (double)O[(ti * 16 + i) * 128 + tj * 16 + j];
+                    s = __dadd_rn(s, __dmul_rn(v, v));
+                }
+            tile_sums[(size_t)((r0 >> 4) + ti) * (size_t)(cols / 16) + (c0 >> 4) + tj] = s;
+        }
+    }
+    if (t == 0) {
+        // after a wait gave up, loads issued later may still be in flight: wait
+        // (bounded) for the last load of each stage before the block exits.
+        // Stage s served iterations s, s + 2, ...: ceil((it - s) / 2) loads.
+        if (gave_up) {
+            for (int s = 0; s < 2; s++) {
+                const int n = (it - s + 1) / 2;
+                if (n <= 0)
+                    continue;
+                unsigned long long t0, t1;
+                asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
+                do {
+                    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
+                } while (!bar_test(bar0 + 8u * (uint32_t)s, (uint32_t)(n - 1) & 1u) && t1 - t0 < kWaitLimitNs);
+            }
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against
+// the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// row-major [rows, cols] matrix, box of box_c columns x box_r rows
+bool encode_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *ptr, int64_t rows,
+                int64_t cols, uint32_t box_c, uint32_t box_r, CUtensorMapSwizzle swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    const cuuint32_t box[2] = {box_c, box_r};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool rotate_fwd_tma_eligible(const RotateLaunch &p) {
+    auto al16 = [](const void *q) { return ((uintptr_t)q & 15u) == 0; };
+    return !p.inverse && p.src == SRC_BF16 && !p.ref && p.out && al16(p.in) && al16(p.out) &&
+           al16(p.sv) && al16(p.su) && p.rows % 128 == 0 && p.cols % 128 == 0 && p.rows < (1ll << 30) &&
+           p.cols < (1ll << 30) && tensor_map_encoder() != nullptr;
+}
+
+// EXL3_OK when launched; EXL3_ERR_UNSUPPORTED when a tensor map cannot be
+// encoded for these pointers (the caller then uses rotate_fwd_kernel).
+exl3_status launch_rotate_fwd_tma(const RotateLaunch &p, cudaStream_t s) {
+    const int64_t nblk = (p.rows / 128) * (p.cols / 128);
+    if (nblk == 0)
+        return EXL3_OK;
+    CUtensorMap in_map, out_map;
+    if (!encode_map(&in_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.in, p.rows, p.cols, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map(&out_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, p.rows, p.cols, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+        return EXL3_ERR_UNSUPPORTED;
+    const size_t smem = kSmemBytes + 1024;   // + alignment slack
+    cudaError_t e = cudaFuncSetAttribute(rotate_fwd_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaFuncSetAttribute(rotate_fwd_tma)");
+    const int64_t grid = nblk < device_sm_count() ? nblk : device_sm_count();
+    rotate_fwd_tma_kernel<<<(unsigned)grid, kTmaThreads, smem, s>>>(in_map, out_map, p.su, p.sv, (int)p.rows,
+                                                                     (int)p.cols, p.tile_sums);
+    note_launch();
+    return cuda_check(cudaGetLastError(), "rotate_fwd_tma launch");
+}
+
+exl3_status rot_take_wait_timeouts(unsigned int *n) {
+    *n = 0;
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_rot_wait_timeouts, sizeof v);
+    if (e == cudaSuccess && v != 0)
+        e = cudaMemcpyToSymbol(g_rot_wait_timeouts, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return cuda_check(e, "wait timeout count");
+    *n = v;
+    return EXL3_OK;
+}
+
+}  // namespace exl3
