@@ -403,15 +403,16 @@ EXL3_API exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launch
                               int64_t *kernel_launches);
 
 /*
- * Device-side wait accounting (no counterpart on the pages).  At K = 1 the
- * two blocks of an encode cluster wait on each other's pushed costs once per
- * trellis step; each such wait gives up after one second, after which the
- * block stops waiting for the rest of the launch and that launch's codes and
- * costs are void.  exl3_wait_timeouts synchronises the device, stores in
- * *count_out (may be NULL) the number of expired waits since the previous call
- * and resets it; it returns EXL3_ERR_TIMEOUT when that number is nonzero,
- * EXL3_ERR_CUDA when the device could not be read, else EXL3_OK.  The count is
- * global to the process and the current device.
+ * Device-side wait accounting (no counterpart on the pages).  Two kernels wait
+ * on asynchronous arrivals: at K = 1 the two blocks of an encode cluster wait on
+ * each other's pushed costs once per trellis step, and the forward rotation of
+ * bf16 weights waits for its TMA tile loads.  Each such wait gives up after one
+ * second, after which the block stops waiting for the rest of the launch and
+ * that launch's results are void.  exl3_wait_timeouts synchronises the device,
+ * stores in *count_out (may be NULL) the number of expired waits since the
+ * previous call and resets it; it returns EXL3_ERR_TIMEOUT when that number is
+ * nonzero, EXL3_ERR_CUDA when the device could not be read, else EXL3_OK.  The
+ * count is global to the process and the current device.
  */
 EXL3_API exl3_status exl3_wait_timeouts(unsigned int *count_out);
 
