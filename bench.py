@@ -48,10 +48,10 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # for the source it was taken on.
 ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu + encode_common.cuh + common.cuh -> DRAM bytes (read +
-    # write) per tile at K=2, from `ncu --set full` on 1,216 tiles of N(0, 1) targets
-    # (profile case `encode`); the traffic is the decision rows, proportional to the
-    # tiles processed.
-    "a0edf80318fa56e3c1274a1b04655209b9c106594b6098ea592ddc1f2f2732d1": 1546270.0,
+    # write) per tile at K=2, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
+    # on 1,216 tiles of N(0, 1) targets (profile case `encode`); the traffic is the
+    # decision rows, proportional to the tiles processed.
+    "c71e4a2c30ece1f527139dc0395d9ec75186e3f5dbc44cd97d129636961db727": 1545464.0,
 }
 
 WORKLOAD = "linear4096_k2"

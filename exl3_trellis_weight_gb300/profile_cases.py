@@ -6,8 +6,11 @@
     python -m exl3_trellis_weight_gb300.profile_cases regularize --rows 4096 --cols 4096
     python -m exl3_trellis_weight_gb300.profile_cases ldl --rows 4096
     python -m exl3_trellis_weight_gb300.profile_cases ldlq --rows 1024 --cols 4096 --K 2
+    python -m exl3_trellis_weight_gb300.profile_cases rows --rows 65536 --cols 160 --K 2
 
 encode  : exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1.
+rows    : exl3_encode_rows on fp32 N(0,1) targets: --rows rows of --cols (= T)
+          targets each, scale 1.
 rotate  : exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix.
 alu-mix : build and run microbench/alu_mix.cu (instruction issue rates per SM
           per clock of the kinds the encoder uses).
@@ -36,7 +39,7 @@ def main(argv=None) -> int:
     from exl3_trellis_weight_gb300 import build, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["encode", "rotate", "alu-mix", "regularize", "ldl", "ldlq"])
+    ap.add_argument("case", choices=["encode", "rows", "rotate", "alu-mix", "regularize", "ldl", "ldlq"])
     ap.add_argument("--K", type=int, default=2)
     ap.add_argument("--rows", type=int, default=1216)
     ap.add_argument("--cols", type=int, default=256)
@@ -57,6 +60,11 @@ def main(argv=None) -> int:
         ws = torch.empty(ex.encode_workspace_bytes(n, a.K), dtype=torch.uint8, device=dev)
         codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
         fn = lambda: ex.encode_tiles(Y, a.K, 1.0, codes=codes, ws=ws)
+    elif a.case == "rows":
+        Y = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+        ws = torch.empty(ex.encode_workspace_bytes(a.rows, a.K), dtype=torch.uint8, device=dev)
+        codes = torch.empty(a.rows, a.cols * a.K // 16, dtype=torch.int16, device=dev)
+        fn = lambda: ex.encode_rows(Y, a.K, 1.0, codes=codes, ws=ws)
     elif a.case == "regularize":
         W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
         h = inputs.hessian_diag(a.rows, 0).to(dev)
