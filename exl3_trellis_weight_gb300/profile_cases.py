@@ -19,7 +19,10 @@ regularize : exl3_regularize of a bf16 N(0, 0.02^2) matrix with a synthetic
 ldl     : exl3_block_ldl of inputs.spd_hessian(rows) (rho 0.95).
 ldlq    : exl3_ldlq of fp32 N(0, 1) targets with the factor of
           inputs.spd_hessian(rows), scale 1.
-Each launch case runs --reps launches and synchronises; it prints the wall time.
+Each launch case runs --reps launches and synchronises; it prints the time per
+launch from CUDA events on the current stream (and the wall time).  --copies N
+(rotate) cycles N distinct input/output pairs, so that with N x 96 MiB above the
+L2 size each launch reads its input from DRAM.
 """
 from __future__ import annotations
 
@@ -44,6 +47,7 @@ def main(argv=None) -> int:
     ap.add_argument("--rows", type=int, default=1216)
     ap.add_argument("--cols", type=int, default=256)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--copies", type=int, default=1)
     a = ap.parse_args(argv)
     if a.case == "alu-mix":
         import subprocess
@@ -87,16 +91,29 @@ def main(argv=None) -> int:
             codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
             fn = lambda: ex.ldlq(R, M, a.K, 1.0, want_q=False, codes=codes, ws=wq)
     else:
-        W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
+        Ws = [inputs.linear_bf16(a.rows, a.cols, c).to(dev) for c in range(a.copies)]
         su, sv = (t.to(dev) for t in inputs.sign_pair(a.rows, a.cols, 0))
-        out = torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev)
-        fn = lambda: ex.rotate(W, su, sv, out=out)
+        outs = [torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev) for _ in range(a.copies)]
+        turn = [0]
+
+        def fn():
+            c = turn[0] % a.copies
+            turn[0] += 1
+            return ex.rotate(Ws[c], su, sv, out=outs[c])
+    if a.copies > 1:
+        for _ in range(2 * a.copies):
+            fn()                                    # warm-up: every copy resident once
     torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
+    ev0.record()
     for _ in range(a.reps):
         fn()
+    ev1.record()
     torch.cuda.synchronize()
-    print(f"{a.case}: {a.reps} launches, {1e3 * (time.perf_counter() - t0) / a.reps:.3f} ms each")
+    wall = 1e3 * (time.perf_counter() - t0) / a.reps
+    print(f"{a.case}: {a.reps} launches, {ev0.elapsed_time(ev1) / a.reps:.4f} ms each (events), "
+          f"{wall:.3f} ms each (wall)")
     return 0
 
 
