@@ -328,6 +328,25 @@ def test_full_linear4096_k2_sampled(ex):
     assert 0 < m < float(W.float().var())
 
 
+@pytest.mark.parametrize("wl,proj,band", [("linear4096_k2", None, 17), ("mlp12288_t5_k4", None, 61),
+                                          ("layer4096_k3", "gate", 40)])
+def test_full_size_one_whole_band(ex, wl, proj, band):
+    """Every tile of one 128-row band (2,048 tiles) of a full-size workload, coded in
+    the benchmark's launch configuration, equals the oracle bit for bit."""
+    (_, W, su, sv, K), = [w for w in inputs.workload(wl) if proj is None or w[0] == proj]
+    rows, cols = W.shape
+    res = ex.quantize(W.to(DEV), su.to(DEV), sv.to(DEV), K, g=1.0)
+    torch.cuda.synchronize()
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    s, inv = oracle.scale_for(1.0, oracle.rms(R))
+    assert float(res["scale"].item()) == s
+    tc = cols // 16
+    idx = np.arange(band * 8 * tc, (band + 1) * 8 * tc, dtype=np.int64)
+    assert idx[-1] < _tiles_of(rows, cols)
+    want, _ = _oracle_codes(R, K, inv, tiles=idx)
+    assert np.array_equal(_np_codes(res["codes"], K)[idx], want)
+
+
 def test_full_mlp12288_k4_sampled(ex):
     (_, W, su, sv, K), = inputs.workload("mlp12288_t5_k4")
     _check_full(ex, W, su, sv, K, 24, 2)
