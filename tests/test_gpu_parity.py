@@ -385,7 +385,10 @@ def test_full_gss4096_k2(ex):
     R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
     s, inv = oracle.scale_for(best_g, oracle.rms(R))
     assert float(res["scale"].item()) == s
-    idx = _sample_tiles(_tiles_of(*W.shape), 16, 4)
+    # 16 sampled tiles plus every tile of one whole 128-row band at the chosen scale
+    tc = W.shape[1] // 16
+    band = np.arange(23 * 8 * tc, 24 * 8 * tc, dtype=np.int64)
+    idx = np.unique(np.concatenate([_sample_tiles(_tiles_of(*W.shape), 16, 4), band]))
     want, _ = _oracle_codes(R, K, inv, tiles=idx)
     assert np.array_equal(_np_codes(res["codes"], K)[idx], want)
 
