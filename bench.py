@@ -592,6 +592,9 @@ def run_ours(args):
                "sample": f"{n_s} seeded random tiles of the rotated {WORKLOAD} matrix, trellis "
                          f"encode only (rotation/rms done once before timing), {dt:.1f} s wall"}
 
+    # bounded device waits that gave up anywhere in this run (K=1 clusters, TMA
+    # rotation): nonzero means some results above are void; read after all timing
+    wait_timeouts = ex.wait_timeouts()
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -612,6 +615,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,
+            "wait_timeouts": wait_timeouts,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
