@@ -179,8 +179,10 @@ def test_rotate_in_place_fp32(ex):
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_rotate_forward_unaligned_views(ex, dt):
     """Inputs and outputs that are not 16-byte aligned take the shuffle-based
-    kernel; aligned ones the shared-memory one: both give the oracle's bits,
-    including non-unit sign vectors (su, sv multiplied as given)."""
+    kernel; 16-byte aligned fp32 inputs the shared-memory one; 16-byte aligned
+    bf16 inputs the TMA one, also from a base that is only 16-byte aligned: all
+    give the oracle's bits, including non-unit sign vectors (su, sv multiplied as
+    given)."""
     rows, cols = 128, 384
     W = inputs.linear_bf16(rows, cols, seed=11, std=0.02)
     if dt == "f32":
@@ -194,7 +196,13 @@ def test_rotate_forward_unaligned_views(ex, dt):
     Wu.copy_(W.to(DEV))
     obuf = torch.empty(n + 8, dtype=torch.float32, device=DEV)
     out_u = obuf[2:2 + n].view(rows, cols)              # 8-byte offset
-    for src, out in ((W.to(DEV), None), (Wu, None), (W.to(DEV), out_u), (Wu, out_u)):
+    buf16 = torch.empty(n + 8, dtype=W.dtype, device=DEV)
+    W16 = buf16[(8 if dt == "bf16" else 4):][:n].view(rows, cols)   # 16-byte offset
+    W16.copy_(W.to(DEV))
+    obuf16 = torch.empty(n + 8, dtype=torch.float32, device=DEV)
+    out16 = obuf16[4:4 + n].view(rows, cols)            # 16-byte offset
+    for src, out in ((W.to(DEV), None), (Wu, None), (W.to(DEV), out_u), (Wu, out_u),
+                     (W16, out16), (W16, None), (W.to(DEV), out16)):
         R = ex.rotate(src, su.to(DEV), sv.to(DEV), out=out)
         torch.cuda.synchronize()
         assert np.array_equal(R.cpu().numpy().view(np.uint32), want.view(np.uint32))
