@@ -10,10 +10,24 @@ encoder) is timed live with CUDA events the library records around each of its
 launches during the timed steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --case encode|rows|rotate|regularize|ldl|ldlq [--K K]
+                    [--rows R] [--cols C] [--reps N] [--copies N]
 
 Under torchrun each rank quantizes its own copy of the workload (weak scaling,
 no collective on the data path); the reported time is the maximum over ranks.
 --impl reference times the CPU oracle on the host cores instead.
+
+--case runs a few launches of one kernel family on a small synthetic case and
+prints their CUDA-event time, no JSON line; it is the command the profiler
+summaries quote:
+  encode     exl3_encode_tiles on fp32 N(0,1) targets (already rotated), scale 1;
+  rows       exl3_encode_rows: --rows rows of --cols (= T) N(0,1) targets, scale 1;
+  rotate     exl3_rotate (forward) of a bf16 N(0, 0.02^2) matrix; --copies N cycles
+             N distinct input/output pairs so that each launch reads from DRAM;
+  regularize exl3_regularize of a bf16 N(0, 0.02^2) matrix with a synthetic
+             Hessian diagonal;
+  ldl        exl3_block_ldl of a synthetic SPD Hessian of order --rows (rho 0.95);
+  ldlq       exl3_ldlq of fp32 N(0,1) targets with that Hessian's factor, scale 1.
 """
 from __future__ import annotations
 
@@ -624,6 +638,79 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# single-kernel cases for profiler captures
+# ---------------------------------------------------------------------------
+
+def run_case(a):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import exl3_trellis_weight_gb300 as ex
+    from exl3_trellis_weight_gb300 import inputs
+    dev = torch.device("cuda:0")
+    if a.case == "encode":
+        Y = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+        n = (a.rows // 16) * (a.cols // 16)
+        ws = torch.empty(ex.encode_workspace_bytes(n, a.K), dtype=torch.uint8, device=dev)
+        codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
+        fn = lambda: ex.encode_tiles(Y, a.K, 1.0, codes=codes, ws=ws)
+    elif a.case == "rows":
+        Y = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+        ws = torch.empty(ex.encode_workspace_bytes(a.rows, a.K), dtype=torch.uint8, device=dev)
+        codes = torch.empty(a.rows, a.cols * a.K // 16, dtype=torch.int16, device=dev)
+        fn = lambda: ex.encode_rows(Y, a.K, 1.0, codes=codes, ws=ws)
+    elif a.case == "regularize":
+        W = inputs.linear_bf16(a.rows, a.cols, 0).to(dev)
+        h = inputs.hessian_diag(a.rows, 0).to(dev)
+        sv = inputs.signs(a.cols, 2).to(dev)
+        out = torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev)
+        ws = torch.empty(ex.regularize_workspace_bytes(a.rows, a.cols), dtype=torch.uint8, device=dev)
+        fn = lambda: ex.regularize(W, h, sv, W_out=out, ws=ws)
+    elif a.case in ("ldl", "ldlq"):
+        H = inputs.spd_hessian(a.rows, 0, rho=0.95).to(dev)
+        M = torch.empty(a.rows, a.rows, dtype=torch.float32, device=dev)
+        wl = torch.empty(ex.block_ldl_workspace_bytes(a.rows), dtype=torch.uint8, device=dev)
+        ex.block_ldl(H, M=M, ws=wl)
+        if a.case == "ldl":
+            fn = lambda: ex.block_ldl(H, M=M, ws=wl)
+        else:
+            del wl
+            R = inputs.iid_f32(a.rows, a.cols, 0).to(dev)
+            wq = torch.empty(ex.ldlq_workspace_bytes(a.rows, a.cols, a.K), dtype=torch.uint8,
+                             device=dev)
+            codes = torch.empty(a.rows // 16, a.cols // 16, 16 * a.K, dtype=torch.int16, device=dev)
+            fn = lambda: ex.ldlq(R, M, a.K, 1.0, want_q=False, codes=codes, ws=wq)
+    else:
+        Ws = [inputs.linear_bf16(a.rows, a.cols, c).to(dev) for c in range(a.copies)]
+        su, sv = (t.to(dev) for t in inputs.sign_pair(a.rows, a.cols, 0))
+        outs = [torch.empty(a.rows, a.cols, dtype=torch.float32, device=dev) for _ in range(a.copies)]
+        turn = [0]
+
+        def fn():
+            c = turn[0] % a.copies
+            turn[0] += 1
+            return ex.rotate(Ws[c], su, sv, out=outs[c])
+    if a.copies > 1:
+        for _ in range(2 * a.copies):
+            fn()                                    # warm-up: every copy resident once
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record()
+    for _ in range(a.reps):
+        fn()
+    ev1.record()
+    torch.cuda.synchronize()
+    wall = 1e3 * (time.perf_counter() - t0) / a.reps
+    print(f"{a.case}: {a.reps} launches, {ev0.elapsed_time(ev1) / a.reps:.4f} ms each (events), "
+          f"{wall:.3f} ms each (wall)")
+    if ex.wait_timeouts() != 0:
+        print("bounded device waits expired: the launches above are void")
+        return 1
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -633,7 +720,15 @@ def main():
     ap.add_argument("--skip-k4", action="store_true")
     ap.add_argument("--skip-aux", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--case", choices=["encode", "rows", "rotate", "regularize", "ldl", "ldlq"])
+    ap.add_argument("--K", type=int, default=2)
+    ap.add_argument("--rows", type=int, default=1216)
+    ap.add_argument("--cols", type=int, default=256)
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--copies", type=int, default=1)
     args = ap.parse_args()
+    if args.case:
+        return run_case(args)
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
