@@ -12,7 +12,9 @@
 // blocks (3 MiB each, 24 MiB in total).  It is created when the library's code
 // is loaded on a device and stays allocated on every device that loads the
 // library until the process exits.  Its host-side name is only a stand-in: the
-// device address is looked up once per device with cudaGetSymbolAddress.
+// device address is looked up with cudaGetSymbolAddress once per device (again
+// after that device's context was destroyed and re-created).  K = 1, whose
+// tiles run on two-block clusters, is not offered here.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,10 +31,50 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[(size_t)kNoAllocMaxB
                                                             sizeof(uint32_t)];
 
 std::mutex g_mu;
-uint32_t *g_addr[kMaxDevices] = {};
+
+// Per device: the context the address was looked up in, and the address.  A
+// device's primary context is destroyed by cudaDeviceReset and the array's
+// address in the next context may differ, so the cache is keyed by the
+// driver's unique context id (0 = not looked up yet).
+struct ScratchSlot {
+    unsigned long long ctx_id;
+    uint32_t *addr;
+};
+ScratchSlot g_slot[kMaxDevices] = {};
+
+typedef int (*PFN_ctx_get_current)(void **ctx);                   // cuCtxGetCurrent
+typedef int (*PFN_ctx_get_id)(void *ctx, unsigned long long *id);  // cuCtxGetId
+
+// The current context's unique id through the driver entry points the runtime
+// hands out (no link against libcuda); 0 when there is no current context yet.
+exl3_status current_context_id(unsigned long long *id) {
+    static PFN_ctx_get_current get_current = nullptr;
+    static PFN_ctx_get_id get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *p1 = nullptr, *p2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 4000,
+                                                          cudaEnableDefault, &q1);
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000,
+                                                          cudaEnableDefault, &q2);
+        if (e1 != cudaSuccess || e2 != cudaSuccess || q1 != cudaDriverEntryPointSuccess ||
+            q2 != cudaDriverEntryPointSuccess || !p1 || !p2)
+            return set_error(EXL3_ERR_CUDA, "driver entry points cuCtxGetCurrent/cuCtxGetId "
+                                            "are not available");
+        get_current = reinterpret_cast<PFN_ctx_get_current>(p1);
+        get_id = reinterpret_cast<PFN_ctx_get_id>(p2);
+    }
+    void *ctx = nullptr;
+    if (get_current(&ctx) != 0)
+        return set_error(EXL3_ERR_CUDA, "cuCtxGetCurrent failed");
+    *id = 0;
+    if (ctx && get_id(ctx, id) != 0)
+        return set_error(EXL3_ERR_CUDA, "cuCtxGetId failed");
+    return EXL3_OK;
+}
 
 // Device address of the scratch array for the current device (set-up on the
-// first call per device).
+// first call per device and context).
 exl3_status scratch_address(uint32_t **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -41,14 +83,23 @@ exl3_status scratch_address(uint32_t **out) {
     if (dev < 0 || dev >= kMaxDevices)
         return set_error(EXL3_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_addr[dev]) {
+    unsigned long long ctx = 0;
+    exl3_status st = current_context_id(&ctx);
+    if (st != EXL3_OK)
+        return st;
+    if (ctx == 0 || g_slot[dev].ctx_id != ctx || !g_slot[dev].addr) {
         void *p = nullptr;
+        // also makes the device's primary context current when none was yet
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess)
             return cuda_check(e, "cudaGetSymbolAddress(noalloc scratch)");
-        g_addr[dev] = static_cast<uint32_t *>(p);
+        st = current_context_id(&ctx);
+        if (st != EXL3_OK)
+            return st;
+        g_slot[dev].ctx_id = ctx;
+        g_slot[dev].addr = static_cast<uint32_t *>(p);
     }
-    *out = g_addr[dev];
+    *out = g_slot[dev].addr;
     return EXL3_OK;
 }
 

@@ -22,10 +22,15 @@
  *     is enqueued on it; no entry point synchronises the host with the device,
  *     except exl3_block_ldl, whose damping retries depend on a device result,
  *     and the exl3_wait_timeouts query.
- *   - The library allocates no device memory.  Scratch comes from the caller's
- *     workspace `ws` (device, 256-byte aligned) of `ws_bytes` bytes, sized with
- *     the matching *_workspace_bytes query.  The workspace must not be used by
- *     anything else until the enqueued work has finished.
+ *   - The library allocates no device memory at run time.  Scratch comes from
+ *     the caller's workspace `ws` (device, 256-byte aligned) of `ws_bytes`
+ *     bytes, sized with the matching *_workspace_bytes query.  The workspace
+ *     must not be used by anything else until the enqueued work has finished.
+ *     The one exception is the static scratch array of
+ *     exl3_encode_tiles_noalloc (about 24 MiB, see there): it is part of the
+ *     library's device code, reserved on a device when that code is loaded
+ *     there (with lazy module loading, at the first call that needs it) and
+ *     held until the process exits.
  *   - Every argument is checked before anything is enqueued; on a non-OK
  *     status nothing was enqueued (except EXL3_ERR_CUDA, which reports a
  *     failed launch) and no output is promised.  exl3_last_error() returns a
@@ -61,8 +66,8 @@ typedef enum {
     EXL3_ERR_UNSUPPORTED = 2,  /* K outside the built set, dims not multiples of 16/128 */
     EXL3_ERR_WORKSPACE = 3,    /* ws_bytes below the minimum for this call */
     EXL3_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-    EXL3_ERR_NUMERIC = 5,      /* the input has no factorisation (exl3_block_ldl) */
-    EXL3_ERR_TIMEOUT = 6       /* a bounded device-side wait expired (exl3_wait_timeouts) */
+    EXL3_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (exl3_wait_timeouts) */
+    EXL3_ERR_NUMERIC = 6       /* the input has no factorisation (exl3_block_ldl) */
 } exl3_status;
 
 typedef enum { EXL3_F32 = 0, EXL3_BF16 = 1 } exl3_dtype;
@@ -80,9 +85,9 @@ EXL3_API int exl3_version(void);
 EXL3_API int exl3_supports_k(int K);
 
 /*
- * Blockwise randomized Hadamard rotation (README item 7: natural-order
- * Sylvester H_128, applied per 128 rows and per 128 columns; decode order
- * H_l -> x su -> H_r -> x sv).
+ * Blockwise randomized Hadamard rotation (page "EXL3 Intel Arc Quantizer",
+ * Core item 7: natural-order Sylvester H_128, applied per 128 rows and per 128
+ * columns; decode order H_l -> x su -> H_r -> x sv).
  *
  *   inverse = 0:  out = 2^-7 * H (su . W . sv) H, in the order
  *                 x sv (columns), rows x H, x su (rows), H x columns, x 2^-7.
@@ -111,9 +116,10 @@ EXL3_API size_t exl3_encode_workspace_bytes(int64_t n_tiles, int K);
 EXL3_API size_t exl3_encode_workspace_min_bytes(int K);
 
 /*
- * Trellis-encode every 16x16 tile of Y (README item 1: two-pass tail-biting
- * Viterbi; item 4: 65536 >> K tracked states, candidates sigma = (k<<(16-K))|e,
- * predecessor sigma >> K, strict-< first-branch ties; item 5: mul1 codebook,
+ * Trellis-encode every 16x16 tile of Y (page "EXL3 Intel Arc Quantizer",
+ * Core item 1: two-pass tail-biting Viterbi; item 4: 65536 >> K tracked
+ * states, candidates sigma = (k<<(16-K))|e, predecessor sigma >> K, strict-<
+ * first-branch ties; item 5: mul1 codebook,
  * MSB-first packing with SWAP16).
  *
  *   Y      (device) fp32 [rows, cols], the rotated matrix; targets are
@@ -139,7 +145,8 @@ EXL3_API exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t col
                               void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Decode packed codes back to tile values (README item 5: state = circular
+ * Decode packed codes back to tile values (page "EXL3 Intel Arc Quantizer", Core
+ * item 5: state = circular
  * 16-bit window, mul1 decode; item 7: values x scale before the inverse
  * rotation).  Yhat[r, c] = fl(v(s) * scale), v the fp16 mul1 level of s.
  *   codes (device, 4-byte aligned) as produced by exl3_encode_tiles.
@@ -150,8 +157,8 @@ EXL3_API exl3_status exl3_decode_tiles(const uint16_t *codes, int64_t rows, int6
 
 /*
  * Row-wise variants for tiles that are not 16x16: every row of Y[n_rows, T]
- * is one tile of T targets (README item 1: "standard L=256 tiles, and L=160
- * n-gram rows").  Same two-pass search, codebook and packing as
+ * is one tile of T targets (page "EXL3 Intel Arc Quantizer", Core item 1,
+ * Shape Support: standard 256-element tiles and 160-element n-gram rows).  Same two-pass search, codebook and packing as
  * exl3_encode_tiles, with the pass-1 roll T/2 and a T*K-bit circular stream
  * per row stored as T*K/16 uint16 words (MSB first, SWAP16).
  *   T even, 16 <= T <= 256, (T*K) % 32 == 0 (e.g. T = 160 for K = 2, 3, 4).
@@ -167,8 +174,8 @@ EXL3_API exl3_status exl3_decode_rows(const uint16_t *codes, int64_t n_rows, int
                                       float scale, float *Yhat, void *stream);
 
 /*
- * Reconstruction MSE (README item 10): sum over tiles of the fp64 squared
- * error sum((double)W - (double)What)^2, each tile summed sequentially in
+ * Reconstruction MSE (page "EXL3 Intel Arc Quantizer", Core item 10): sum over
+ * tiles of the fp64 squared error sum((double)W - (double)What)^2, each tile summed sequentially in
  * row-major order and the tile sums added as a pairwise tree (neighbours
  * (2i, 2i+1) per level, an odd last element moving up), divided by rows*cols.
  *   W (device) dtype dt [rows, cols];  What (device) fp32 [rows, cols].
@@ -182,7 +189,8 @@ EXL3_API exl3_status exl3_mse(const void *W, int dt, const float *What, int64_t 
 /*
  * One full quantization at relative scale g (all of the above in order):
  * R = rotate(W); sigma = sqrt(tree(tile sums of R^2) / n) in fp64, taken as
- * 1 when it is 0 (an all-zero matrix); s = fl32(g * sigma); codes = encode(R, s); What = inverse(decode(codes, s));
+ * 1 when it is 0 (an all-zero matrix); s = fl32(g * sigma); codes = encode(R, s);
+ * What = inverse(decode(codes, s));
  * mse = MSE(W, What).
  *   W (device) bf16 or fp32 [rows, cols]; su, sv (device) fp32 sign vectors.
  *   rows, cols multiples of 128; K in {1, 2, 3, 4}; g > 0.
@@ -205,8 +213,9 @@ EXL3_API exl3_status exl3_quantize(const void *W, int dt, int64_t rows, int64_t 
                           void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Golden-section search over the relative scale g in [lo, hi] (JEV-9B model
- * card, section 2: "Golden Section Search (GSS) scale optimization"), every
+ * Golden-section search over the relative scale g in [lo, hi] (page
+ * "alpha2beta/JEV-9B-EXL3-K2", section 2: "Golden Section Search (GSS) scale
+ * optimization"), every
  * evaluation a full exl3_quantize.  With phi = (sqrt 5 - 1)/2 in fp64:
  * x1 = b - phi(b-a), x2 = a + phi(b-a), both evaluated; then while fewer than
  * n_eval evaluations: if f(x1) <= f(x2) {b = x2; x2 = x1; x1 = b - phi(b-a);
@@ -229,11 +238,12 @@ EXL3_API exl3_status exl3_gss_scale(const void *W, int dt, int64_t rows, int64_t
                            void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Grid-and-parabola global-scale search on a tile sample (README item 8:
+ * Grid-and-parabola global-scale search on a tile sample (page "EXL3 Intel Arc
+ * Quantizer", Core item 8:
  * wrapped-diagonal tile sampling with the highest/lowest-RMS tiles, coarse grid
  * 0.1..1.9 on a strided subsample, fine grid within 0.075 of the coarse
  * minimum on the full sample, parabolic refinement with a 0.01 floor).  The
- * README leaves the details open; this library reads them as follows.
+ * page leaves the details open; this library reads them as follows.
  *   sample   : tiles (i mod TR, i mod TC) for i < max(TR, TC) (TR x TC 16x16
  *              tiles of R = rotate(W)), then the highest- and lowest-RMS tiles
  *              (ties to the lower index) when not already in the sample;
@@ -262,8 +272,8 @@ EXL3_API exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int6
                                        size_t ws_bytes, void *stream);
 
 /*
- * Block LDL factorisation of a Hessian (README item 3: blockwise Cholesky/LDL,
- * the inverse of the 16x16 block diagonal folded in, retry-only damping of
+ * Block LDL factorisation of a Hessian (page "EXL3 Intel Arc Quantizer", Core
+ * item 3: blockwise Cholesky/LDL, the inverse of the 16x16 block diagonal folded in, retry-only damping of
  * 2 sigma_reg mean(diag H) up to 10 times).
  *   H = L L^T (binary64 Cholesky in the textbook order: each entry
  *   H[i][j] - sum_{k<j} L[i][k] L[j][k], k ascending, one rounded product and
@@ -275,8 +285,8 @@ EXL3_API exl3_status exl3_scale_search(const void *W, int dt, int64_t rows, int6
  *   whose pivots are all > 0 is kept.
  *   H (device) double [n, n] row-major, symmetric: only the lower triangle is
  *     read; n a multiple of 16 in [16, 32768].
- *   sigma_reg >= 0 and finite (0.01 in the README's damping); max_retries in
- *     [0, 100] (10 in the README).
+ *   sigma_reg >= 0 and finite (0.01 in the page's damping); max_retries in
+ *     [0, 100] (10 on the page).
  *   M (device, 16-byte aligned) float [n, n] out: fl32 of M's strictly lower
  *     block part (the entries below the 16x16 diagonal blocks); the diagonal
  *     blocks (identity) and everything above them are written as 0.  Each
@@ -295,8 +305,8 @@ EXL3_API exl3_status exl3_block_ldl(const double *H, int64_t n, double sigma_reg
 
 /*
  * LDLQ: trellis-code the 16-row spans of R bottom-up with error feedback
- * (README item 3: one-sided LDLQ error feedback, the tile encoder as the
- * callback on each span).  With E = fl32(R - Q) for the spans already coded
+ * (page "EXL3 Intel Arc Quantizer", Core item 3: one-sided LDLQ error
+ * feedback, the tile encoder as the callback on each span).  With E = fl32(R - Q) for the spans already coded
  * (Q = fl32(v * scale)), span b (rows 16b .. 16b+15) is coded from the
  * targets U_b = fl32(R_b + acc_b), where acc_b[r][c] is the binary32 chain
  * acc = fmaf(M[i][16b + r], E[i][c], acc) over i = rows-1 down to 16(b+1)
@@ -323,11 +333,12 @@ EXL3_API exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const
                                void *stream);
 
 /*
- * Output-channel regularisation of a weight before rotation (README item 8:
+ * Output-channel regularisation of a weight before rotation (page "EXL3 Intel Arc
+ * Quantizer", Core item 8:
  * block_rms with a 32-slice accumulation order, the output-scale skew
  * heuristic on the top 2 % of sqrt(H_diag) against a 15 % cutoff, output-channel
  * RMS normalisation with sign and scale folded into sv, and the zero-channel
- * floor 0.1 with sv = 0).  The README names the parts only; this library reads
+ * floor 0.1 with sv = 0).  The page names the parts only; this library reads
  * them as follows.
  *   S_c      : the rows cut into 32 consecutive slices of ceil(rows / 32) rows;
  *              each slice's binary64 sum of w^2 in row order; the slice sums
@@ -366,22 +377,26 @@ EXL3_API exl3_status exl3_regularize(const void *W, int dt, int64_t rows, int64_
  * owns all device memory through its own pool, and latency-critical loops that
  * cannot afford an allocation (cudaMalloc may synchronise the whole device).
  *
- * Same inputs, outputs, layout and results as exl3_encode_tiles; the decision
- * rows live in a static device array inside the library instead of a caller
- * workspace.  That array holds at most EXL3_NOALLOC_MAX_BLOCKS persistent
- * blocks (8 blocks x 3,137,536 bytes, about 24 MiB) and stays allocated on every
- * device that loads the library until the process exits.
+ * Same inputs, outputs, layout and results as exl3_encode_tiles for K in
+ * {2, 3, 4}; K = 1 (whose tiles run on two-block clusters) is not offered here
+ * and returns EXL3_ERR_UNSUPPORTED.  The decision rows live in a static device
+ * array inside the library instead of a caller workspace.  That array holds at
+ * most EXL3_NOALLOC_MAX_BLOCKS persistent blocks (8 blocks x 3,137,536 bytes,
+ * about 24 MiB) and stays allocated on every device that loads the library's
+ * device code until the process exits.
  *   blocks: number of persistent blocks to run, 1..EXL3_NOALLOC_MAX_BLOCKS, or
  *           0 for the maximum.  More is rejected with EXL3_ERR_WORKSPACE.
  *           With at most 8 of the GPU's SMs busy this is slower than
  *           exl3_encode_tiles with a full-machine workspace.
- * The first call on each device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  The function allocates nothing and creates no CUDA events.  All
- * calls share the one array: calls whose work overlaps on the GPU (for example
- * on two streams without ordering) race and produce wrong codes.  Nothing in
- * the array needs clearing between calls: each call writes every decision row
- * before reading it.
+ * Set-up: the first call on each device (and the first after that device's
+ * context was destroyed, e.g. by cudaDeviceReset) looks up the array's device
+ * address with that device current; with lazy module loading that first call
+ * also loads the library's device code.  Make that first call before any
+ * stream capture.  The function allocates nothing and creates no CUDA events.
+ * All calls share the one array: calls whose work overlaps on the GPU (for
+ * example on two streams without ordering) race and produce wrong codes.
+ * Nothing in the array needs clearing between calls: each call writes every
+ * decision row before reading it.
  */
 #define EXL3_NOALLOC_MAX_BLOCKS 8
 EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_t rows, int64_t cols, int K,

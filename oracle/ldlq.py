@@ -9,7 +9,8 @@ M = L * blockdiag(L_bb)^-1, diagonal damping of 2 * sigma_reg * mean(diag H)
 retried up to 10 times, and one-sided error feedback that walks the weight's
 16-row spans bottom-up, adding to each span's targets the errors of the spans
 already quantised, weighted by the strictly lower part of M.  The page states
-no more than that; the readings (also in the design notes):
+no more than that; the readings below fill in the rest, each a choice made
+where the page is silent:
 
   * weights are R [n, cols] (rows = input channels, the Hessian's index), the
     Hessian H [n, n] is symmetric positive definite in the same basis;

@@ -7,7 +7,8 @@ item 8 ("Weight Regularization & Global-Scale Search"): block_rms with a
 32-slice accumulation order, the output-scale skew heuristic (the top 2 % of
 sqrt(H_diag) against a 15 % cutoff), output-channel RMS normalisation, sign and
 scale folded into sv, and the zero-channel floor 0.1 with sv = 0.  The page
-names these parts only; the readings (also in the design notes):
+names these parts only; the readings below fill in the rest, each a choice
+made where the page is silent:
 
   * W [rows, cols] has the input channels down the rows (the Hessian's index)
     and the output channels across; H_diag [rows] is the Hessian's diagonal;

@@ -7,8 +7,8 @@ item 8: the global scale is searched on a wrapped-diagonal sample of tiles plus
 the highest- and lowest-RMS tiles, first on a coarse grid 0.1..1.9 over a
 strided subsample, then on a fine grid within 0.075 of the coarse minimum over
 the full sample, then refined by a parabola with a 0.01 floor.  The page gives
-no more than that; the readings below fill in the rest (also listed in the
-design notes):
+no more than that; the readings below fill in the rest, each a choice made
+where the page is silent:
 
   * tiles are the 16x16 tiles of the rotated matrix R, TR x TC of them;
   * wrapped diagonal: tile (i mod TR, i mod TC) for i = 0 .. max(TR, TC) - 1;

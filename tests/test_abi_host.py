@@ -43,7 +43,8 @@ def test_status_strings(ex):
     L = ex.lib()
     assert L.exl3_status_str(0) == b"EXL3_OK"
     assert L.exl3_status_str(3) == b"EXL3_ERR_WORKSPACE"
-    assert L.exl3_status_str(6) == b"EXL3_ERR_TIMEOUT"
+    assert L.exl3_status_str(5) == b"EXL3_ERR_TIMEOUT"
+    assert L.exl3_status_str(6) == b"EXL3_ERR_NUMERIC"
     assert L.exl3_status_str(99) == b"EXL3_ERR_UNKNOWN"
     assert L.exl3_version() >= 100
 

@@ -5,8 +5,9 @@ plug-ins inside an application that owns all device memory through its own
 pool, or latency-critical loops that cannot afford an allocation.  It keeps the
 encoder's decision rows in a static device array of the library instead of a
 caller workspace.  Its codes and tile costs must equal those of
-exl3_encode_tiles bit for bit, on consecutive calls that reuse the same static
-array.  The file is named so that pytest collects it last.
+exl3_encode_tiles and of the CPU oracle bit for bit, on consecutive calls that
+reuse the same static array.  The file is named so that pytest collects it
+last.
 """
 import ctypes
 
@@ -14,6 +15,9 @@ import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from exl3_trellis_weight_gb300 import inputs  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -55,14 +59,20 @@ def test_noalloc_matches_workspace_encode_on_consecutive_calls(lib):
         (96, 160, 4, 0.8, 3, 2),
     ]
     for rows, cols, K, scale, blocks, seed in cases:
-        g = torch.Generator().manual_seed(seed)
-        Y = torch.randn(rows, cols, generator=g).to(dev)
+        Yc = inputs.iid_f32(rows, cols, seed)
+        Y = Yc.to(dev)
         codes_n, cost_n = _noalloc(L, Y, K, scale, blocks)
         codes_w, cost_w = ex.encode_tiles(Y, K, scale, want_cost=True)
         torch.cuda.synchronize()
         assert torch.equal(codes_n, codes_w)
         assert np.array_equal(cost_n.cpu().numpy().view(np.uint32),
                               cost_w.cpu().numpy().view(np.uint32))
+        # and against the oracle: targets fl(Y * fl32(1 / scale))
+        inv = float(np.float32(1.0) / np.float32(scale))
+        st, costs_o = oracle.encode_matrix(Yc.numpy(), K, inv)
+        codes_o = np.stack([oracle.pack(s, K) for s in st])
+        assert np.array_equal(codes_n.cpu().numpy().view(np.uint16).reshape(-1, 16 * K), codes_o)
+        assert np.array_equal(cost_n.cpu().numpy().view(np.uint32), costs_o.view(np.uint32))
 
 
 def test_noalloc_rejects_more_blocks_than_the_static_array_holds(lib):
@@ -73,3 +83,16 @@ def test_noalloc_rejects_more_blocks_than_the_static_array_holds(lib):
                                      ctypes.c_void_p(codes.data_ptr()), None, MAX_BLOCKS + 1, None)
     assert st == 3   # EXL3_ERR_WORKSPACE
     assert b"at most" in L.exl3_last_error()
+
+
+def test_noalloc_rejects_k1(lib):
+    """K = 1 tiles run on two-block clusters, which this entry point does not
+    offer: it returns EXL3_ERR_UNSUPPORTED and enqueues nothing."""
+    _, L = lib
+    Y = torch.zeros(16, 16, device="cuda:0")
+    codes = torch.full((1, 1, 16), 7, dtype=torch.int16, device="cuda:0")
+    st = L.exl3_encode_tiles_noalloc(ctypes.c_void_p(Y.data_ptr()), 16, 16, 1, ctypes.c_float(1.0),
+                                     ctypes.c_void_p(codes.data_ptr()), None, 0, None)
+    assert st == 2   # EXL3_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((codes == 7).all())
