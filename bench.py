@@ -201,6 +201,82 @@ def oracle_time(R, K, inv, idx, threads):
     return time.perf_counter() - t0
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_workload_targets(name: str):
+    """(R, K, inv_scale) of a named workload at g = 1, from the oracle's own rotation."""
+    import oracle
+    from exl3_trellis_weight_gb300 import inputs
+    (_, W, su, sv, K), = inputs.workload(name)
+    if su is None:                       # already rotated, fixed scale 1.0
+        return W.numpy(), K, 1.0
+    R = oracle.rotate_forward(W.float().numpy(), su.numpy(), sv.numpy())
+    _, inv = oracle.scale_for(1.0, oracle.rms(R))
+    return R, K, inv
+
+
+def cpu_baseline(n_tiles: int = 1024):
+    """The oracle's tile-encode rate on this host's cores (rank 0, one GPU only).
+
+    Single-thread: every tile of the 128x128 K=2 matrix, and a fixed seeded
+    subset of n_tiles tiles of the 4096x4096 K=2 and of the 12288x4096 K=4
+    workloads (targets at g = 1).  The three run side by side, one host thread
+    each.  Multi-thread: the same 4096x4096 subset over all host cores.
+    Rotation and rms are done before timing; the time is the trellis encode.
+    """
+    import threading
+    import numpy as np
+    import oracle
+    oracle.build()
+    nproc = oracle.default_threads()
+    cases = [("rot128_iid_k2", None), ("linear4096_k2", n_tiles), ("mlp12288_t5_k4", n_tiles)]
+    prep = []
+    for name, k in cases:
+        R, K, inv = _oracle_workload_targets(name)
+        n_all = (R.shape[0] // 16) * (R.shape[1] // 16)
+        idx = (np.arange(n_all) if k is None
+               else np.sort(np.random.default_rng(2024).choice(n_all, k, replace=False)))
+        prep.append((name, R, K, inv, idx))
+    single = {}
+
+    def one(name, R, K, inv, idx):
+        t0 = time.perf_counter()
+        oracle.encode_matrix(R, K, inv, tiles=idx, threads=1)
+        dt = time.perf_counter() - t0
+        single[name] = {"tiles": int(idx.size), "K": K, "seconds": round(dt, 2),
+                        "tiles_per_s": idx.size / dt}
+
+    th = [threading.Thread(target=one, args=p) for p in prep]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    _, R2, K2, inv2, idx2 = prep[1]
+    t0 = time.perf_counter()
+    oracle.encode_matrix(R2, K2, inv2, tiles=idx2, threads=nproc)
+    dt = time.perf_counter() - t0
+    value = idx2.size / dt
+    return {"value": value, "unit": UNIT, "cores": nproc, "kind": "oracle",
+            "cpu": _cpu_model(),
+            "sample": (f"trellis encode of a fixed seeded subset of {idx2.size} tiles of the rotated "
+                       f"{WORKLOAD} matrix (g = 1) over {nproc} host threads, {dt:.1f} s wall; "
+                       f"rotation and rms done before timing"),
+            "single_thread": single,
+            "single_thread_note": ("one host thread per workload, the three side by side on "
+                                   "separate cores; 128x128 = all 64 tiles, the others a fixed "
+                                   f"seeded {n_tiles}-tile subset")}
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -596,15 +672,7 @@ def run_ours(args):
     # ---- CPU baseline (rank 0, one GPU only) ---------------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        import oracle
-        oracle.build()
-        threads = oracle.default_threads()
-        n_s = max(8 * threads, 64)
-        Rn, Kc, inv, idx = oracle_sample_setup(n_s, seed=7)
-        dt = oracle_time(Rn, Kc, inv, idx, threads)
-        cpu = {"value": n_s / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{n_s} seeded random tiles of the rotated {WORKLOAD} matrix, trellis "
-                         f"encode only (rotation/rms done once before timing), {dt:.1f} s wall"}
+        cpu = cpu_baseline(args.cpu_tiles)
 
     # bounded device waits that gave up anywhere in this run (K=1 clusters, TMA
     # rotation): nonzero means some results above are void; read after all timing
@@ -720,6 +788,8 @@ def main():
     ap.add_argument("--skip-k4", action="store_true")
     ap.add_argument("--skip-aux", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-tiles", type=int, default=1024,
+                    help="tiles in each timed oracle subset of the CPU baseline")
     ap.add_argument("--case", choices=["encode", "rows", "rotate", "regularize", "ldl", "ldlq"])
     ap.add_argument("--K", type=int, default=2)
     ap.add_argument("--rows", type=int, default=1216)
