@@ -21,7 +21,7 @@ __all__ = [
     "encode_rows", "decode_rows",
     "quantize", "gss_scale", "scale_search", "scale_search_workspace_bytes", "encode_workspace_bytes", "encode_workspace_min_bytes",
     "quantize_workspace_bytes", "gss_workspace_bytes", "mse_workspace_bytes",
-    "supports_k", "profile_enable", "profile_read", "wait_timeouts", "EXL3_F32", "EXL3_BF16",
+    "supports_k", "rotate_last_kernel", "profile_enable", "profile_read", "wait_timeouts", "EXL3_F32", "EXL3_BF16",
 ]
 
 EXL3_F32 = 0
@@ -96,6 +96,8 @@ def lib():
         L.exl3_profile_enable.restype = None
         L.exl3_profile_read.argtypes = [P, P, P]
         L.exl3_wait_timeouts.argtypes = [P]
+        L.exl3_rotate_last_kernel.argtypes = []
+        L.exl3_rotate_last_kernel.restype = i32
         for name in ("exl3_regularize", "exl3_block_ldl", "exl3_ldlq", "exl3_scale_search", "exl3_encode_rows", "exl3_decode_rows", "exl3_profile_read", "exl3_wait_timeouts", "exl3_rotate", "exl3_encode_tiles", "exl3_decode_tiles", "exl3_mse",
                      "exl3_quantize", "exl3_gss_scale"):
             getattr(L, name).restype = i32
@@ -178,6 +180,12 @@ def wait_timeouts() -> int:
     if st not in (0, 5):
         _check(st)
     return int(n.value)
+
+
+def rotate_last_kernel() -> int:
+    """exl3_rotate_last_kernel: 1 TMA forward, 2 shared-memory forward, 3 warp-shuffle
+    kernel, 0 none -- the kernel the calling thread's last rotation launched."""
+    return int(lib().exl3_rotate_last_kernel())
 
 
 def supports_k(K: int) -> bool:

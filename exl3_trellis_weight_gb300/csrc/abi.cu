@@ -51,6 +51,11 @@ constexpr size_t kMaxEv = 4096;
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// kernel of the calling thread's most recent rotation launch (exl3_rotate_last_kernel)
+static thread_local int t_rot_kernel = 0;
+void note_rotate_kernel(int which) { t_rot_kernel = which; }
+int last_rotate_kernel() { return t_rot_kernel; }
+
 void profile_encode_begin(cudaStream_t s) {
     t_open = nullptr;
     if (!g_prof_on.load(std::memory_order_relaxed))
@@ -403,6 +408,8 @@ const char *exl3_status_str(int status) {
 }
 
 const char *exl3_last_error(void) { return g_err; }
+
+int exl3_rotate_last_kernel(void) { return exl3::last_rotate_kernel(); }
 
 int exl3_version(void) { return 100; }
 

@@ -145,6 +145,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // launch accounting for exl3_profile_* (abi.cu)
 void note_launch();
+// records which kernel a rotation launched: 1 TMA forward, 2 shared-memory
+// forward, 3 warp-shuffle (inverse, decode-fused or unaligned)
+void note_rotate_kernel(int which);
+int last_rotate_kernel();
 void profile_encode_begin(cudaStream_t s);
 void profile_encode_end(cudaStream_t s);
 

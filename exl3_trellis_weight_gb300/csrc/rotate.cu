@@ -301,6 +301,7 @@ exl3_status launch_rotate(const RotateLaunch &p, cudaStream_t s) {
         return cuda_check(e, "cudaFuncSetAttribute(rotate)");
     rotate_kernel<<<(unsigned)nblk, kRotThreads, smem, s>>>(p);
     note_launch();
+    note_rotate_kernel(3);
     return cuda_check(cudaGetLastError(), "rotate launch");
 }
 

@@ -205,6 +205,7 @@ exl3_status launch_rotate_fwd(const RotateLaunch &p, cudaStream_t s) {
         return cuda_check(e, "cudaFuncSetAttribute(rotate_fwd)");
     rotate_fwd_kernel<<<(unsigned)nblk, kFwdThreads, smem, s>>>(p);
     note_launch();
+    note_rotate_kernel(2);
     return cuda_check(cudaGetLastError(), "rotate_fwd launch");
 }
 

@@ -144,17 +144,30 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         gave_up = 0;
     }
     __syncthreads();
-    if (t == 0 && (int)blockIdx.x < nblk)
+    // loads issued per input stage (thread 0's count; every load is waited on
+    // before the next one on the same stage is issued, so at most one is in
+    // flight per stage and each barrier is at most one phase behind)
+    int issued0 = 0, issued1 = 0;
+    if (t == 0 && (int)blockIdx.x < nblk) {
         issue_load(&in_map, su, sv, base, bar0, (int)blockIdx.x, nbc);
+        issued0 = 1;
+    }
 
     int it = 0;
     for (int blk = (int)blockIdx.x; blk < nblk; blk += (int)gridDim.x, it++) {
         const int st = it & 1;
         const int r0 = (blk / nbc) * 128, c0 = (blk % nbc) * 128;
-        // the other stage was last read in the previous block's phase 1
-        if (t == 0 && blk + (int)gridDim.x < nblk)
+        // the other stage was last read in the previous block's phase 1 and its
+        // load was waited on there; after a wait gave up no load is issued any
+        // more (a second arrival on a barrier phase still in flight is not allowed)
+        if (t == 0 && blk + (int)gridDim.x < nblk && !gave_up) {
             issue_load(&in_map, su, sv, base + (uint32_t)(st ^ 1) * kStageBytes,
                        bar0 + 8u * (uint32_t)(st ^ 1), blk + (int)gridDim.x, nbc);
+            if (st)
+                issued0++;
+            else
+                issued1++;
+        }
         bar_wait(bar0 + 8u * (uint32_t)st, (uint32_t)(it >> 1) & 1u, &gave_up);
 
         // ---- phase 1: row i, columns 32 jh .. 32 jh + 31 -> j spans 1..16 -------
@@ -265,19 +278,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
     }
     if (t == 0) {
-        // after a wait gave up, loads issued later may still be in flight: wait
-        // (bounded) for the last load of each stage before the block exits.
-        // Stage s served iterations s, s + 2, ...: ceil((it - s) / 2) loads.
+        // after a wait gave up, the last load of each stage may still be in
+        // flight: wait (bounded) for it before the block exits, so that no copy
+        // lands in shared memory of a block that is gone.  Stage s has completed
+        // phases 0 .. n - 1 (n loads issued on it) once that load has landed.
         if (gave_up) {
             for (int s = 0; s < 2; s++) {
-                const int n = (it - s + 1) / 2;
-                if (n <= 0)
+                const int n = s ? issued1 : issued0;
+                if (n == 0)
                     continue;
+                const uint32_t parity = (uint32_t)(n - 1) & 1u;
                 unsigned long long t0, t1;
                 asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
                 do {
                     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
-                } while (!bar_test(bar0 + 8u * (uint32_t)s, (uint32_t)(n - 1) & 1u) && t1 - t0 < kWaitLimitNs);
+                } while (!bar_test(bar0 + 8u * (uint32_t)s, parity) && t1 - t0 < kWaitLimitNs);
             }
         }
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -350,6 +365,7 @@ exl3_status launch_rotate_fwd_tma(const RotateLaunch &p, cudaStream_t s) {
     rotate_fwd_tma_kernel<<<(unsigned)grid, kTmaThreads, smem, s>>>(in_map, out_map, p.su, p.sv, (int)p.rows,
                                                                      (int)p.cols, p.tile_sums);
     note_launch();
+    note_rotate_kernel(1);
     return cuda_check(cudaGetLastError(), "rotate_fwd_tma launch");
 }
 

@@ -404,6 +404,16 @@ EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_t rows, int
                                                int blocks, void *stream);
 
 /*
+ * Which kernel the calling thread's most recent exl3_rotate (or the rotation
+ * inside exl3_quantize) launched (no counterpart on the pages; a test hook):
+ * 1 the TMA forward kernel (bf16 weights, 16-byte aligned pointers), 2 the
+ * shared-memory forward kernel (fp32 weights, or when no tensor map could be
+ * encoded), 3 the warp-shuffle kernel (inverse, decode-fused, or pointers that
+ * are not 16-byte aligned), 0 none yet.  Thread-local; no synchronisation.
+ */
+EXL3_API int exl3_rotate_last_kernel(void);
+
+/*
  * Profiling (no counterpart on the pages; used by the benchmark).  While
  * enabled, each launch of the encode kernel is bracketed by two CUDA events
  * recorded on its stream, and every kernel launch made by the library is

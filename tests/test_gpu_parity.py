@@ -201,9 +201,16 @@ def test_rotate_forward_unaligned_views(ex, dt):
     W16.copy_(W.to(DEV))
     obuf16 = torch.empty(n + 8, dtype=torch.float32, device=DEV)
     out16 = obuf16[4:4 + n].view(rows, cols)            # 16-byte offset
+    def kernel_for(src, out):
+        al16 = src.data_ptr() % 16 == 0 and (out is None or out.data_ptr() % 16 == 0)
+        if not al16:
+            return 3                                     # warp-shuffle kernel
+        return 1 if dt == "bf16" else 2                  # TMA (bf16) / shared-memory (fp32)
+
     for src, out in ((W.to(DEV), None), (Wu, None), (W.to(DEV), out_u), (Wu, out_u),
                      (W16, out16), (W16, None), (W.to(DEV), out16)):
         R = ex.rotate(src, su.to(DEV), sv.to(DEV), out=out)
+        assert ex.rotate_last_kernel() == kernel_for(src, out)
         torch.cuda.synchronize()
         assert np.array_equal(R.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
