@@ -24,6 +24,12 @@
 //     fwd1(A) | tb2(prev B);  fwd1(B) | tb1(A);  fwd2(A) | tb1(B);  fwd2(B) | tb2(A)
 // where thread 0 performs one traceback step per forward step, issuing the
 // load at the start of the step and consuming it at the end.
+//
+// At K = 3 and 4 the cost rows of two tiles fit one SM's shared memory, and
+// encode2_kernel runs the same pipeline on pairs of tiles: every barrier
+// interval holds the step of both tiles of a pair (6-7 % faster than one tile
+// per interval on 4096 x 4096), with the decision rows packed so that the two
+// pairs in flight use the same per-block workspace slice.
 #include "encode_common.cuh"
 
 namespace exl3 {
@@ -289,6 +295,323 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     }
 }
 
+// ---------------------------------------------------------------------------
+// K = 3, 4: two tiles per forward pass.  The cost rows of both fit one SM's
+// shared memory (2 tiles x 2 buffers x 2^(16-K) fp32), so each barrier
+// interval runs the step of tile x = 0 and then of tile x = 1: twice the work
+// per barrier, and one tile's comparisons overlap the other's loads and
+// squares.  The pipeline is the one above with "unit" = a pair of tiles:
+//     fwd1(P) | tb2(prev Q);  fwd1(Q) | tb1(P);  fwd2(P) | tb1(Q);  fwd2(Q) | tb2(P)
+// with the two tracebacks of a pair run by threads 0 and 32.  Decision rows
+// are packed to the bits a step produces (K = 4: one word per thread, 512 per
+// row; K = 3: two 24-bit fields per thread, 768 words per row) so that the two
+// pairs in flight (one region of 2 x 255 rows each) fit the same per-block
+// workspace slice as the single-tile pipeline.
+// ---------------------------------------------------------------------------
+template <int K>
+struct Dual {
+    static constexpr int RW = K == 3 ? 768 : 512;        // words per decision row
+    static constexpr size_t SLOT = (size_t)kRowsPass2 * RW; // one tile's rows
+    static_assert(4 * SLOT * sizeof(uint32_t) <= kEncodeBlockScratchBytes, "rows fit the slice");
+    // bit offset of D_t(g) in a row
+    __device__ __forceinline__ static uint32_t bit_of(uint32_t g) {
+        const uint32_t hp = g >> K, j = g & (uint32_t)((1 << K) - 1);
+        if (K == 3) {
+            const uint32_t tid = hp & 511u, u = hp >> 9;
+            return 48u * tid + 24u * u + 3u * j;
+        }
+        // K = 4: word hp * 2 + j / 8, bit (j % 8) * 4
+        return 32u * (hp * 2u + (j >> 3)) + 4u * (j & 7u);
+    }
+};
+
+template <int K>
+__device__ __forceinline__ void dual_store_row(uint32_t *row, const uint32_t (&word)[Geo<K>::DW],
+                                               const int tid) {
+    if constexpr (K == 4) {
+        row[tid] = word[0];
+    } else {
+        // 48 bits per thread: unit 0 at bits 0..23, unit 1 at 24..47; thread pair
+        // (2m, 2m + 1) fills words 3m .. 3m + 2 (the odd thread's low 16 bits
+        // complete the even thread's second word)
+        const unsigned long long v = (unsigned long long)word[0] | ((unsigned long long)word[1] << 24);
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, (uint32_t)v & 0xFFFFu, 1);
+        const int m = tid >> 1;
+        if ((tid & 1) == 0) {
+            row[3 * m] = (uint32_t)v;
+            row[3 * m + 1] = (uint32_t)(v >> 32) | (recv << 16);
+        } else {
+            row[3 * m + 2] = (uint32_t)(v >> 16);
+        }
+    }
+}
+
+struct Tb2 {         // one traceback of the dual pipeline (threads 0 and 32)
+    const uint32_t *rows;
+    int tile;
+    uint32_t s;
+    unsigned long long pending;
+    int t, stop, row0, pass;
+    bool on;
+};
+
+template <int K>
+__device__ __forceinline__ void tb2_issue(Tb2 &tb) {
+    const uint32_t off = Dual<K>::bit_of(tb.s >> K);
+    const uint32_t *r = tb.rows + (size_t)(tb.t - 1 - tb.row0) * Dual<K>::RW + (off >> 5);
+    if (K == 3) {
+        const uint32_t lo = __ldcg(r);
+        const uint32_t hi = ((off & 31u) > 29u) ? __ldcg(r + 1) : 0u;
+        tb.pending = (unsigned long long)lo | ((unsigned long long)hi << 32);
+    } else {
+        tb.pending = __ldcg(r);
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void tb2_advance(Tb2 &tb, uint32_t *bs) {
+    using Gm = Geo<K>;
+    const uint32_t g = tb.s >> K;
+    const uint32_t off = Dual<K>::bit_of(g);
+    const uint32_t k = (uint32_t)(tb.pending >> (off & 31u)) & (uint32_t)(Gm::NK - 1);
+    tb.s = (k << Gm::KR) | g;
+    tb.t -= 1;
+    if (tb.pass == 2)
+        put_code<K>(bs, tb.t, tb.s & (uint32_t)(Gm::NK - 1));
+    if (tb.t == tb.stop)
+        tb.on = false;
+}
+
+template <int K, int TT>
+__global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch a) {
+    using Gm = Geo<K>;
+    using Du = Dual<K>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *Mb = reinterpret_cast<float *>(smem);                  // [x][buffer][G]
+    float *ysb = Mb + 4 * Gm::G;                                   // [x][256]
+    uint32_t *bsb = reinterpret_cast<uint32_t *>(ysb + 512);       // [x][32]
+    unsigned long long *red = reinterpret_cast<unsigned long long *>(bsb + 64);   // [32]
+    __shared__ uint32_t sh_sstar[2][2], sh_end[2][2];             // [unit slot][x]
+    __shared__ Tb2 tbs[2];
+
+    const int tid = threadIdx.x;
+    const int my_tb = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
+
+    uint32_t vpk[Gm::STATES / 2];
+#pragma unroll
+    for (int u = 0; u < Gm::NU; u++)
+#pragma unroll
+        for (int k = 0; k < Gm::NK; k++)
+#pragma unroll
+            for (int jj = 0; jj < Gm::NJ; jj += 2) {
+                const uint32_t g = ((uint32_t)Gm::unit(u, tid) << K) | (uint32_t)(Gm::j0(tid) + jj);
+                const uint32_t s0 = ((uint32_t)k << Gm::KR) | g;
+                const unsigned short h0 = __half_as_ushort(mul1_half(s0));
+                const unsigned short h1 = __half_as_ushort(mul1_half(s0 + 1u));
+                vpk[((u * Gm::NK + k) * Gm::NJ + jj) >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            }
+
+    const float inv_s = a.inv_scale_dev ? __ldg(a.inv_scale_dev) : a.inv_scale;
+    const int T = TT ? TT : a.T;
+    const int half = T / 2;
+    const int code_words = T * K / 32;
+    const bool row_tiles = TT == 0;
+    const int tiles_c = row_tiles ? 1 : (int)(a.cols / 16);
+    const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
+    const int grid = (int)gridDim.x;
+    const int n_my = (isfinite(inv_s) && n_tiles > (int)blockIdx.x)
+                         ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
+    const int n_units = (n_my + 1) / 2;                  // pairs of tiles
+    uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
+
+    if (my_tb >= 0) {
+        Tb2 &tb = tbs[my_tb];
+        tb.on = false;
+        tb.rows = nullptr;
+        tb.tile = 0;
+        tb.s = 0u;
+        tb.pending = 0ull;
+        tb.t = tb.stop = tb.row0 = tb.pass = 0;
+    }
+
+    const int nq = (n_units + 1) / 2;
+    for (int ph = 0; ph <= nq * 4; ph++) {
+        const int p = ph >> 2;
+        const int sub = ph & 3;
+        int f_slot = 0, f_pass = 0, b_slot = 0, b_pass = 0;
+        int f_loc = -1, b_loc = -1;
+        if (p < nq) {
+            const int A = 2 * p, B = 2 * p + 1;
+            const bool hasB = B < n_units;
+            if (sub == 0) {
+                f_slot = 0; f_pass = 1; f_loc = A;
+                if (p > 0) { b_slot = 1; b_pass = 2; b_loc = 2 * p - 1; }
+            } else if (sub == 1) {
+                if (hasB) { f_slot = 1; f_pass = 1; f_loc = B; }
+                b_slot = 0; b_pass = 1; b_loc = A;
+            } else if (sub == 2) {
+                f_slot = 0; f_pass = 2; f_loc = A;
+                if (hasB) { b_slot = 1; b_pass = 1; b_loc = B; }
+            } else {
+                if (hasB) { f_slot = 1; f_pass = 2; f_loc = B; }
+                b_slot = 0; b_pass = 2; b_loc = A;
+            }
+        } else if (p > 0 && 2 * p - 1 < n_units) {
+            b_slot = 1; b_pass = 2; b_loc = 2 * p - 1;
+        }
+        const bool fwd = f_loc >= 0;
+        // tiles of a unit: local indices 2 * unit + x
+        const bool has1 = fwd && 2 * f_loc + 1 < n_my;
+
+        if (fwd) {
+            for (int x = 0; x < (has1 ? 2 : 1); x++) {
+                const int f_tile = (int)blockIdx.x + (2 * f_loc + x) * grid;
+                float *ys = ysb + 256 * x;
+                if (tid < T) {
+                    const int i = (f_pass == 1) ? (tid + half < T ? tid + half : tid + half - T) : tid;
+                    const float *src;
+                    if (row_tiles) {
+                        src = a.Y + (size_t)f_tile * (size_t)T + i;
+                    } else {
+                        const int tr = f_tile / tiles_c, tc = f_tile % tiles_c;
+                        src = a.Y + (size_t)(tr * 16 + (i >> 4)) * (size_t)a.cols + tc * 16 + (i & 15);
+                    }
+                    ys[tid] = __fmul_rn(__ldg(src), inv_s);
+                }
+                float *M0 = Mb + (size_t)(2 * x) * Gm::G;
+                if (f_pass == 1) {
+                    for (int g = tid; g < Gm::G; g += kThreads)
+                        M0[g] = 0.0f;
+                } else {
+                    const int ge = (int)(sh_end[f_slot][x] & (uint32_t)(Gm::G - 1));
+                    for (int g = tid; g < Gm::G; g += kThreads)
+                        M0[g] = (g == ge) ? 0.0f : __int_as_float(0x7f800000);
+                }
+            }
+        }
+        const bool has_b1 = b_loc >= 0 && 2 * b_loc + 1 < n_my;
+        if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
+            Tb2 &tb = tbs[my_tb];
+            uint32_t *bs = bsb + 32 * my_tb;
+            tb.on = true;
+            tb.pass = b_pass;
+            tb.tile = (int)blockIdx.x + (2 * b_loc + my_tb) * grid;
+            tb.t = T - 1;
+            tb.rows = scr + (size_t)(2 * b_slot + my_tb) * Du::SLOT;
+            if (b_pass == 1) {
+                tb.s = sh_sstar[b_slot][my_tb];
+                tb.stop = half - 1;
+                tb.row0 = half - 1;
+            } else {
+                tb.s = sh_end[b_slot][my_tb];
+                tb.stop = 0;
+                tb.row0 = 0;
+                for (int w = 0; w < code_words; w++)
+                    bs[w] = 0u;
+                put_code<K>(bs, T - 1, tb.s & (uint32_t)(Gm::NK - 1));
+            }
+        }
+        __syncthreads();
+
+        if (fwd) {
+            const int row0 = (f_pass == 1) ? half - 1 : 0;
+            uint32_t *rows0 = scr + (size_t)(2 * f_slot) * Du::SLOT;
+            uint32_t *rows1 = rows0 + Du::SLOT;
+            float *const A0 = Mb, *const A1 = Mb + Gm::G;             // tile 0 buffers
+            float *const B0 = Mb + 2 * Gm::G, *const B1 = Mb + 3 * Gm::G;   // tile 1 buffers
+            for (int t = 0; t < T - 1; t++) {
+                if (my_tb >= 0 && tbs[my_tb].on)
+                    tb2_issue<K>(tbs[my_tb]);
+                uint32_t word[Gm::DW];
+                unsigned long long key = 0ull;
+                acs_step<K, false>((t & 1) ? A1 : A0, (t & 1) ? A0 : A1, ysb[t], vpk, tid, word, key);
+                if (t >= row0)
+                    dual_store_row<K>(rows0 + (size_t)(t - row0) * Du::RW, word, tid);
+                if (has1) {
+                    uint32_t word1[Gm::DW];
+                    acs_step<K, false>((t & 1) ? B1 : B0, (t & 1) ? B0 : B1, ysb[256 + t], vpk, tid, word1, key);
+                    if (t >= row0)
+                        dual_store_row<K>(rows1 + (size_t)(t - row0) * Du::RW, word1, tid);
+                }
+                if (my_tb >= 0 && tbs[my_tb].on)
+                    tb2_advance<K>(tbs[my_tb], bsb + 32 * my_tb);
+                __syncthreads();
+            }
+            if (f_pass == 1) {
+                // step T-1: lowest full state with minimal cost, per tile
+                if (my_tb >= 0 && tbs[my_tb].on)
+                    tb2_issue<K>(tbs[my_tb]);
+                uint32_t word[Gm::DW];
+                unsigned long long key0 = ~0ull, key1 = ~0ull;
+                acs_step<K, true>(A1, nullptr, ysb[T - 1], vpk, tid, word, key0);
+                if (has1)
+                    acs_step<K, true>(B1, nullptr, ysb[256 + T - 1], vpk, tid, word, key1);
+                if (my_tb >= 0 && tbs[my_tb].on)
+                    tb2_advance<K>(tbs[my_tb], bsb + 32 * my_tb);
+                key0 = warp_min_u64(key0);
+                key1 = warp_min_u64(key1);
+                if ((tid & 31) == 0) {
+                    red[tid >> 5] = key0;
+                    red[16 + (tid >> 5)] = key1;
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    unsigned long long k = red[tid];   // lanes 0..15: tile 0, 16..31: tile 1
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) {
+                        const unsigned long long w = __shfl_xor_sync(0xffffffffu, k, o);
+                        k = w < k ? w : k;
+                    }
+                    if (tid == 0)
+                        sh_sstar[f_slot][0] = (uint32_t)(k & 0xffffffffull);
+                    if (tid == 16)
+                        sh_sstar[f_slot][1] = (uint32_t)(k & 0xffffffffull);
+                }
+            } else if (a.tile_cost && (tid == 0 || (tid == 32 && has1))) {
+                const int x = tid == 0 ? 0 : 1;
+                const uint32_t e = sh_end[f_slot][x];
+                const float d = __fsub_rn(ysb[256 * x + T - 1], mul1_value(e));
+                const float *M1x = x ? B1 : A1;
+                a.tile_cost[(int)blockIdx.x + (2 * f_loc + x) * grid] = __fadd_rn(M1x[e >> K], __fmul_rn(d, d));
+            }
+        }
+        if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
+            Tb2 &tb = tbs[my_tb];
+            uint32_t *bs = bsb + 32 * my_tb;
+            while (tb.on) {
+                tb2_issue<K>(tb);
+                tb2_advance<K>(tb, bs);
+            }
+            if (tb.pass == 1) {
+                sh_end[b_slot][my_tb] = tb.s;
+            } else {
+                uint32_t *dst = a.codes + (size_t)tb.tile * code_words;
+                for (int w = 0; w < code_words; w++)
+                    dst[w] = bs[w];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int K, int TT>
+exl3_status launch_dual(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    using Gm = Geo<K>;
+    const size_t smem = (size_t)(4 * Gm::G + 512 + 64) * sizeof(float) + 32 * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(encode2_kernel<K, TT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return cuda_check(e, "cudaFuncSetAttribute(encode2)");
+    if (profiled)
+        profile_encode_begin(s);
+    encode2_kernel<K, TT><<<p.grid, kThreads, smem, s>>>(p);
+    if (profiled) {
+        note_launch();
+        profile_encode_end(s);
+    }
+    return cuda_check(cudaGetLastError(), "encode launch");
+}
+
 template <int K, int TT>
 exl3_status launch_kt(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
@@ -309,6 +632,11 @@ exl3_status launch_kt(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
 
 template <int K>
 exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    if constexpr (K >= 3) {
+        if (p.row_tiles)
+            return launch_dual<K, 0>(p, s, profiled);
+        return launch_dual<K, 256>(p, s, profiled);
+    }
     if (p.row_tiles)
         return launch_kt<K, 0>(p, s, profiled);
     return launch_kt<K, 256>(p, s, profiled);
