@@ -83,6 +83,111 @@ __device__ __forceinline__ void acs_step(const float *__restrict__ Mp, float *__
     }
 }
 
+// Candidates of one entry pair (two entries j, j + 1 of one unit) for the NK
+// predecessors: c[k] = fl(M(k) + fl(fl(v - y)^2)), two packed per 64 bits.
+template <int K>
+__device__ __forceinline__ void cands_pair(const unsigned long long (&mm)[1 << K], const uint32_t *vp,
+                                           const float y, unsigned long long (&c)[1 << K]) {
+#pragma unroll
+    for (int k = 0; k < (1 << K); k++)
+        c[k] = cand2(vp[k * (Geo<K>::NJ / 2)], y, mm[k]);
+}
+
+// Running minimum over k with the lowest k on ties, as a balanced tournament
+// (pairs (0,1), (2,3), ... then their winners): the same result as the
+// sequential scan, with log2 NK dependent levels instead of NK - 1.
+template <int K>
+__device__ __forceinline__ void tour_pair(const unsigned long long (&c)[1 << K], int &best0, int &best1,
+                                          uint32_t &bk0, uint32_t &bk1) {
+    constexpr int NK = 1 << K;
+    int v0[NK], v1[NK];
+    uint32_t i0[NK], i1[NK];
+#pragma unroll
+    for (int k = 0; k < NK; k++) {
+        v0[k] = (int)(uint32_t)(c[k] & 0xffffffffull);
+        v1[k] = (int)(uint32_t)(c[k] >> 32);
+        i0[k] = (uint32_t)k;
+        i1[k] = (uint32_t)k;
+    }
+#pragma unroll
+    for (int w = 1; w < NK; w <<= 1) {
+#pragma unroll
+        for (int k = 0; k < NK; k += 2 * w) {
+            bool keep0, keep1;      // keep: the lower group is no worse
+            v0[k] = __vibmin_s32(v0[k], v0[k + w], &keep0);
+            v1[k] = __vibmin_s32(v1[k], v1[k + w], &keep1);
+            i0[k] = keep0 ? i0[k] : i0[k + w];
+            i1[k] = keep1 ? i1[k] : i1[k + w];
+        }
+    }
+    best0 = v0[0];
+    best1 = v1[0];
+    bk0 = i0[0];
+    bk1 = i1[0];
+}
+// The single-tile kernel's step (K = 2): the same candidates and results as
+// acs_step, with two changes that measured 8.7 % faster at 4096 x 4096
+// (384.6 -> 351.3 ms): the minimum over k is a balanced tournament (lowest k
+// on ties, like the scan, with log2 NK dependent levels instead of NK - 1), and
+// the candidates of the next entry pair are formed before the current pair's
+// comparisons.  At K = 3 and 4 the same form spilled and ran slower.
+template <int K, bool ARGMIN>
+__device__ __forceinline__ void acs_step_sp(const float *__restrict__ Mp, float *__restrict__ Mn,
+                                         const float y, const uint32_t (&vpk)[Geo<K>::STATES / 2],
+                                         const int tid, uint32_t (&word)[Geo<K>::DW],
+                                         unsigned long long &key) {
+    using Gm = Geo<K>;
+    constexpr int NP = Gm::NJ / 2;                 // entry pairs per unit
+    constexpr int NE = Gm::NU * NP;                // entry pairs per thread
+#pragma unroll
+    for (int w = 0; w < Gm::DW; w++)
+        word[w] = 0u;
+    const int j0 = Gm::j0(tid);
+    unsigned long long mm[Gm::NK];
+#pragma unroll
+    for (int k = 0; k < Gm::NK; k++) {
+        const float m = Mp[(k << (16 - 2 * K)) + Gm::unit(0, tid)];
+        mm[k] = pack_costs(m, m);
+    }
+    // software pipeline: the candidates (loads, squares, adds) of entry pair
+    // e + 1 are formed before the comparisons of entry pair e, so that each
+    // warp's instruction stream alternates FMA-pipe and ALU-pipe work
+    unsigned long long cn[Gm::NK];
+    cands_pair<K>(mm, &vpk[0], y, cn);
+    float outv[Gm::NJ];
+#pragma unroll
+    for (int e = 0; e < NE; e++) {
+        const int u = e / NP, jp = 2 * (e % NP);
+        const int hp = Gm::unit(u, tid);
+        unsigned long long cc[Gm::NK];
+#pragma unroll
+        for (int k = 0; k < Gm::NK; k++)
+            cc[k] = cn[k];
+        if (e + 1 < NE) {
+            const int u1 = (e + 1) / NP, jp1 = 2 * ((e + 1) % NP);
+            if (jp1 == 0) {
+#pragma unroll
+                for (int k = 0; k < Gm::NK; k++) {
+                    const float m = Mp[(k << (16 - 2 * K)) + Gm::unit(u1, tid)];
+                    mm[k] = pack_costs(m, m);
+                }
+            }
+            cands_pair<K>(mm, &vpk[((u1 * Gm::NK) * Gm::NJ + jp1) >> 1], y, cn);
+        }
+        int best0 = 0, best1 = 0;
+        uint32_t bk0 = 0u, bk1 = 0u;
+        tour_pair<K>(cc, best0, best1, bk0, bk1);
+        finish_pair<K, ARGMIN>(u, jp, hp, j0, best0, best1, bk0, bk1, outv, word, key);
+        if (!ARGMIN && jp + 2 == Gm::NJ) {
+            float *dst = Mn + (hp << K) + j0;
+#pragma unroll
+            for (int q = 0; q < Gm::NJ; q += 4)
+                *reinterpret_cast<float4 *>(dst + q) =
+                    make_float4(outv[q], outv[q + 1], outv[q + 2], outv[q + 3]);
+        }
+    }
+}
+
 template <int K>
 __device__ __forceinline__ void tb_issue(Tb &tb) {
     int w, b;
@@ -243,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 float *Mn = (t & 1) ? M0 : M1;
                 uint32_t word[Gm::DW];
                 unsigned long long key = 0ull;
-                acs_step<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
+                acs_step_sp<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
                 if (t >= row0) {
 #pragma unroll
                     for (int w = 0; w < Gm::DW; w++)
@@ -259,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                     tb_issue<K>(tb);
                 uint32_t word[Gm::DW];
                 unsigned long long key = ~0ull;
-                acs_step<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
+                acs_step_sp<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
                 if (tid == 0 && tb.on)
                     tb_advance<K>(tb, bs);
                 key = warp_min_u64(key);
@@ -636,10 +741,11 @@ exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
         if (p.row_tiles)
             return launch_dual<K, 0>(p, s, profiled);
         return launch_dual<K, 256>(p, s, profiled);
+    } else {
+        if (p.row_tiles)
+            return launch_kt<K, 0>(p, s, profiled);
+        return launch_kt<K, 256>(p, s, profiled);
     }
-    if (p.row_tiles)
-        return launch_kt<K, 0>(p, s, profiled);
-    return launch_kt<K, 256>(p, s, profiled);
 }
 
 }  // namespace
