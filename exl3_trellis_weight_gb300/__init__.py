@@ -171,10 +171,9 @@ def profile_read():
 
 def wait_timeouts() -> int:
     """exl3_wait_timeouts -> number of bounded device waits that expired since
-    the last call (the K=1 encoder's waits on the peer block's pushed costs and
-    the TMA forward rotation's waits on its tile loads); synchronises the device
-    and resets the count.  A nonzero count means the launches concerned
-    produced void results."""
+    the last call (the TMA forward rotation's waits on its tile loads);
+    synchronises the device and resets the count.  A nonzero count means the
+    launches concerned produced void results."""
     n = ctypes.c_uint(0)
     st = lib().exl3_wait_timeouts(ctypes.byref(n))
     if st not in (0, 5):

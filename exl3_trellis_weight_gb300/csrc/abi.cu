@@ -120,24 +120,18 @@ struct Carver {
     }
 };
 
-// Persistent blocks for the whole machine.  K = 1 runs two-block clusters
-// (one tile per cluster at a time), so its grid is even.
+// Persistent blocks for the whole machine: one per SM (one tile per block at
+// a time; at K = 3 and 4 a pair of tiles).
 int encode_grid_full(int64_t n_tiles, int K) {
+    (void)K;
     const int64_t sm = device_sm_count();
-    if (K == 1) {
-        const int64_t g = 2 * n_tiles;
-        const int64_t smax = sm & ~1ll;
-        return (int)(g < smax ? g : smax);
-    }
     return (int)(n_tiles < sm ? n_tiles : sm);
 }
 
-// Grid that fits `cap` block slices (even for K = 1); 0 if none fits.
+// Grid that fits `cap` block slices; 0 if none fits.
 int64_t fit_blocks(int64_t full, int64_t cap, int K) {
-    int64_t g = full < cap ? full : cap;
-    if (K == 1)
-        g &= ~1ll;
-    return g;
+    (void)K;
+    return full < cap ? full : cap;
 }
 
 struct QuantWs {
@@ -444,11 +438,11 @@ size_t exl3_encode_workspace_bytes(int64_t n_tiles, int K) {
     if (!k_ok(K) || n_tiles < 0)
         return 0;
     const int64_t g = encode_grid_full(n_tiles, K);
-    return (size_t)(g > 0 ? g : (K == 1 ? 2 : 1)) * kEncodeBlockScratchBytes;
+    return (size_t)(g > 0 ? g : 1) * kEncodeBlockScratchBytes;
 }
 
 size_t exl3_encode_workspace_min_bytes(int K) {
-    return k_ok(K) ? (size_t)(K == 1 ? 2 : 1) * kEncodeBlockScratchBytes : 0;
+    return k_ok(K) ? kEncodeBlockScratchBytes : 0;
 }
 
 exl3_status exl3_encode_tiles(const float *Y, int64_t rows, int64_t cols, int K, float scale,
@@ -852,7 +846,7 @@ exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M
     const size_t fixed = ldlq_carve(nullptr, rows, cols, 0, nullptr);
     const int64_t cap = ws_bytes > fixed ? (int64_t)((ws_bytes - fixed) / kEncodeBlockScratchBytes) : 0;
     const int grid = (int)fit_blocks(encode_grid_full(cols / 16, K), cap, K);
-    if (grid < (K == 1 ? 2 : 1))
+    if (grid < 1)
         return set_error(EXL3_ERR_WORKSPACE, "workspace %zu bytes is below the minimum", ws_bytes);
     LdlqLaunch l{};
     ldlq_carve(ws, rows, cols, grid, &l);
@@ -973,7 +967,7 @@ exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launches, int64
 
 exl3_status exl3_wait_timeouts(unsigned int *count_out) {
     unsigned int n = 0, r = 0;
-    exl3_status st = exl3::k1_take_wait_timeouts(&n);   // synchronises the device
+    exl3_status st = exl3::cuda_check(cudaDeviceSynchronize(), "device synchronise (wait timeouts)");
     if (st == EXL3_OK)
         st = exl3::rot_take_wait_timeouts(&r);
     n += r;

@@ -169,10 +169,6 @@ struct EncodeLaunch {
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s);
 // same launch without the profiling hooks (creates no CUDA events)
 exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s);
-// K = 1: two-block clusters (grid even)
-exl3_status launch_encode_k1(const EncodeLaunch &p, cudaStream_t s, bool profiled);
-// synchronises the device, reads and clears the K = 1 expired-wait count
-exl3_status k1_take_wait_timeouts(unsigned int *n);
 
 exl3_status launch_decode(const uint32_t *codes, int64_t rows, int64_t cols, int K,
                           float scale, const float *scale_dev, float *out, cudaStream_t s);

@@ -1,7 +1,8 @@
 // encode.cu -- persistent trellis tile encoder (page "EXL3 Intel Arc
 // Quantizer", Core Implemented Architecture items 1, 4 and 5).
 //
-// One 512-thread block per SM walks its share of the tiles.  A tile is T
+// One 512-thread block per SM walks its share of the tiles (K = 1, 2 here; K =
+// 3, 4 in encode2_kernel below, two tiles at a time).  A tile is T
 // targets: the 256 elements of a 16x16 tile (row-major), or one row of T
 // elements (even T in [16, 256]).  For each tile:
 //   pass 1: targets rolled left by T/2, free start, T add-compare-select
@@ -12,7 +13,8 @@
 //           is forced to end at end_state); traced back from end_state; the
 //           low K bits of each state are packed MSB first.
 //
-// The tracked cost row M (2^(16-K) fp32) is double-buffered in shared memory;
+// The tracked cost row M (2^(16-K) fp32) is double-buffered in shared memory
+// (K = 1: one row, updated in place; see acs_step_k1);
 // the mul1 level of each of a thread's 128 candidate states is fixed for the
 // whole launch and is kept in registers as packed fp16.  Decisions (K bits per
 // tracked entry per step, one or two 32-bit words per thread per step) go to
@@ -188,10 +190,121 @@ __device__ __forceinline__ void acs_step_sp(const float *__restrict__ Mp, float 
     }
 }
 
+// ---------------------------------------------------------------------------
+// K = 1: one block per tile, the 2^15-entry cost row updated in place in one
+// buffer (two would not fit one SM).  Unit h (14 bits) owns the tracked
+// entries 2h and 2h + 1; both read the predecessor costs M(h) (k = 0) and
+// M(h | 2^14) (k = 1).  M_t(g) is kept at position f(rotr^(t+1)(g)), where rotr
+// rotates the 15-bit index right by one and f(p) = p + (p >> 5) + (p >> 10):
+// then f(rotr^(t+1)(2h)) = f(rotr^t(h)) and f(rotr^(t+1)(2h + 1)) =
+// f(rotr^t(h | 2^14)), so the two new costs of unit h land exactly where its
+// two predecessor costs were read.  Each position is read and rewritten by the
+// one thread that owns it at that step, and one barrier per step orders the
+// steps.  The padding f sends the 32 lanes of a warp (units differing in the
+// five low bits, which the rotation moves to any five cyclically adjacent bit
+// positions) to 32 distinct banks at every step; the row takes 33,822 floats.
+// Thread tid owns units h = (i << 9) | tid, i < 32.  The positions split as
+// f(rotr^s(tid)) + f(rotr^s(i << 9)) (+ f(rotr^s(2^14)) for k = 1), s = t mod
+// 15, the middle term a sum of five per-step values; the units are walked in
+// Gray-code order of i, so each unit's address is one add from the previous
+// one's, and their loads are issued BATCH units at a time ahead of the
+// comparisons.
+// ---------------------------------------------------------------------------
+constexpr int kK1RowFloats = 33822;   // f(2^15 - 1) + 1
+
+__host__ __device__ __forceinline__ uint32_t rotr15(uint32_t x, int s) {
+    return ((x >> s) | (x << (15 - s))) & 0x7FFFu;
+}
+__host__ __device__ __forceinline__ uint32_t k1_pad(uint32_t p) { return p + (p >> 5) + (p >> 10); }
+
+// D_t(g) of entry g (15 bits): thread h & 511 of unit h = g >> 1, word i >> 4,
+// bit 2 (i & 15) + (g & 1), with i = h >> 9
+__host__ __device__ __forceinline__ void k1_dec_locate(uint32_t g, int &word, int &bit) {
+    const uint32_t h = g >> 1, i = h >> 9;
+    word = (int)((h & 511u) + 512u * (i >> 4));
+    bit = (int)(((i & 15u) << 1) | (g & 1u));
+}
+
+template <int K>
+__device__ __forceinline__ void dec_loc(uint32_t g, int &w, int &b) {
+    if constexpr (K == 1)
+        k1_dec_locate(g, w, b);
+    else
+        Geo<K>::dec_locate(g, w, b);
+}
+
+// One step at K = 1 (s = t mod 15: M_{t-1}(x) sits at k1_pad(rotr^s(x))).
+template <bool ARGMIN>
+__device__ __forceinline__ void acs_step_k1(float *M, const float y, const uint32_t (&vpk)[64],
+                                            const int tid, const int s, uint32_t (&word)[2],
+                                            unsigned long long &key) {
+    constexpr int BATCH = 4;
+    word[0] = 0u;
+    word[1] = 0u;
+    const uint32_t E0 = k1_pad(rotr15(1u << 9, s)), E1 = k1_pad(rotr15(1u << 10, s)),
+                   E2 = k1_pad(rotr15(1u << 11, s)), E3 = k1_pad(rotr15(1u << 12, s)),
+                   E4 = k1_pad(rotr15(1u << 13, s));
+    const uint32_t D = k1_pad(rotr15(1u << 14, s));
+    uint32_t a0 = k1_pad(rotr15((uint32_t)tid, s));
+    // every position is read, then rewritten, by the one unit that owns it at
+    // this step, and different units' positions never coincide: loads go
+    // through Mr and stores through Mw so that a later unit's loads may move
+    // above an earlier unit's stores (a unit's stores depend on its own loads)
+    const float *__restrict__ Mr = M;
+    float *__restrict__ Mw = M;
+#pragma unroll
+    for (int n0 = 0; n0 < 32; n0 += BATCH) {
+        uint32_t ad0[BATCH], ad1[BATCH];
+        float m0[BATCH], m1[BATCH];
+#pragma unroll
+        for (int q = 0; q < BATCH; q++) {
+            const int n = n0 + q;
+            const int i = n ^ (n >> 1);
+            if (n > 0) {
+                const int b = __ffs(n) - 1;          // the Gray-code bit that flips
+                const uint32_t Eb = b == 0 ? E0 : b == 1 ? E1 : b == 2 ? E2 : b == 3 ? E3 : E4;
+                if (i & (1 << b))
+                    a0 += Eb;
+                else
+                    a0 -= Eb;
+            }
+            ad0[q] = a0;
+            ad1[q] = a0 + D;
+            m0[q] = Mr[ad0[q]];
+            m1[q] = Mr[ad1[q]];
+        }
+#pragma unroll
+        for (int q = 0; q < BATCH; q++) {
+            const int n = n0 + q;
+            const int i = n ^ (n >> 1);
+            const unsigned long long c0 = cand2(vpk[2 * i], y, pack_costs(m0[q], m0[q]));
+            const unsigned long long c1 = cand2(vpk[2 * i + 1], y, pack_costs(m1[q], m1[q]));
+            bool keep0, keep1;   // keep: k = 0 is no worse (ties keep the lower k)
+            const int b0 = __vibmin_s32((int)(uint32_t)(c0 & 0xffffffffull),
+                                        (int)(uint32_t)(c1 & 0xffffffffull), &keep0);
+            const int b1 = __vibmin_s32((int)(uint32_t)(c0 >> 32), (int)(uint32_t)(c1 >> 32), &keep1);
+            const uint32_t bk0 = keep0 ? 0u : 1u, bk1 = keep1 ? 0u : 1u;
+            word[i >> 4] |= (bk0 << ((i & 15) * 2)) | (bk1 << ((i & 15) * 2 + 1));
+            if (ARGMIN) {
+                const uint32_t g0 = 2u * (((uint32_t)i << 9) | (uint32_t)tid);
+                const unsigned long long k0 =
+                    ((unsigned long long)(uint32_t)b0 << 32) | ((bk0 << 15) | g0);
+                const unsigned long long k1 =
+                    ((unsigned long long)(uint32_t)b1 << 32) | ((bk1 << 15) | (g0 + 1u));
+                key = k0 < key ? k0 : key;
+                key = k1 < key ? k1 : key;
+            } else {
+                Mw[ad0[q]] = __int_as_float(b0);
+                Mw[ad1[q]] = __int_as_float(b1);
+            }
+        }
+    }
+}
+
 template <int K>
 __device__ __forceinline__ void tb_issue(Tb &tb) {
     int w, b;
-    Geo<K>::dec_locate(tb.s >> K, w, b);
+    dec_loc<K>(tb.s >> K, w, b);
     tb.pending = __ldcg(tb.rows + (size_t)(tb.t - 1 - tb.row0) * kRowWords + w);
 }
 
@@ -200,7 +313,7 @@ __device__ __forceinline__ void tb_advance(Tb &tb, uint32_t *bs) {
     using Gm = Geo<K>;
     const uint32_t g = tb.s >> K;
     int w, b;
-    Gm::dec_locate(g, w, b);
+    dec_loc<K>(g, w, b);
     const uint32_t k = (tb.pending >> b) & (uint32_t)(Gm::NK - 1);
     tb.s = (k << Gm::KR) | g;
     tb.t -= 1;
@@ -218,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     extern __shared__ __align__(16) unsigned char smem[];
     float *M0 = reinterpret_cast<float *>(smem);
     float *M1 = M0 + Gm::G;
-    float *ys = M1 + Gm::G;                                       // up to 256 targets
+    // K = 1: one row of kK1RowFloats (+ 2 for alignment); M1 is not used
+    float *ys = K == 1 ? M0 + kK1RowFloats + 2 : M1 + Gm::G;     // up to 256 targets
     uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);         // packed codes (tb2)
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
     __shared__ uint32_t sh_sstar[2], sh_end[2];
@@ -228,6 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
 
     // mul1 levels of this thread's candidate states, packed two per register
     uint32_t vpk[Gm::STATES / 2];
+    if constexpr (K == 1) {
+        // vpk[2 i + k] = (v((k << 15) | 2h), v((k << 15) | 2h + 1)), h = (i << 9) | tid
+#pragma unroll
+        for (int i = 0; i < 32; i++)
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const uint32_t s0 = ((uint32_t)k << 15) | (2u * (((uint32_t)i << 9) | (uint32_t)tid));
+                vpk[2 * i + k] = (uint32_t)__half_as_ushort(mul1_half(s0)) |
+                                 ((uint32_t)__half_as_ushort(mul1_half(s0 + 1u)) << 16);
+            }
+    } else
 #pragma unroll
     for (int u = 0; u < Gm::NU; u++)
 #pragma unroll
@@ -305,7 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 }
                 ys[tid] = __fmul_rn(__ldg(src), inv_s);
             }
-            if (f_pass == 1) {
+            if (K == 1 && f_pass == 1) {
+                for (int g = tid; g < kK1RowFloats; g += kThreads)
+                    M0[g] = 0.0f;
+            } else if (K == 1) {
+                // M_{-1}(g) at k1_pad(g)
+                const uint32_t ge = sh_end[f_slot] & 0x7FFFu;
+                for (int g = tid; g < Gm::G; g += kThreads)
+                    M0[k1_pad((uint32_t)g)] = ((uint32_t)g == ge) ? 0.0f : __int_as_float(0x7f800000);
+            } else if (f_pass == 1) {
                 for (int g = tid; g < Gm::G; g += kThreads)
                     M0[g] = 0.0f;
             } else {
@@ -348,7 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 float *Mn = (t & 1) ? M0 : M1;
                 uint32_t word[Gm::DW];
                 unsigned long long key = 0ull;
-                acs_step_sp<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
+                if constexpr (K == 1)
+                    acs_step_k1<false>(M0, ys[t], vpk, tid, t % 15, word, key);
+                else
+                    acs_step_sp<K, false>(Mp, Mn, ys[t], vpk, tid, word, key);
                 if (t >= row0) {
 #pragma unroll
                     for (int w = 0; w < Gm::DW; w++)
@@ -364,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                     tb_issue<K>(tb);
                 uint32_t word[Gm::DW];
                 unsigned long long key = ~0ull;
-                acs_step_sp<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
+                if constexpr (K == 1)
+                    acs_step_k1<true>(M0, ys[T - 1], vpk, tid, (T - 1) % 15, word, key);
+                else
+                    acs_step_sp<K, true>(M1, nullptr, ys[T - 1], vpk, tid, word, key);
                 if (tid == 0 && tb.on)
                     tb_advance<K>(tb, bs);
                 key = warp_min_u64(key);
@@ -380,7 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 // path forced to end at end_state: fl(M_{T-2}(end >> K) + q_{T-1}(end))
                 const uint32_t e = sh_end[f_slot];
                 const float d = __fsub_rn(ys[T - 1], mul1_value(e));
-                a.tile_cost[f_tile] = __fadd_rn(M1[e >> K], __fmul_rn(d, d));
+                const float mprev = K == 1 ? M0[k1_pad(rotr15(e >> 1, (T - 1) % 15))] : M1[e >> K];
+                a.tile_cost[f_tile] = __fadd_rn(mprev, __fmul_rn(d, d));
             }
         }
         if (tid == 0 && b_loc >= 0) {
@@ -720,7 +860,8 @@ exl3_status launch_dual(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
 template <int K, int TT>
 exl3_status launch_kt(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
-    const size_t smem = (size_t)(2 * Gm::G + 256 + 32) * sizeof(float) + 32 * sizeof(unsigned long long);
+    const size_t smem = (size_t)((K == 1 ? kK1RowFloats + 2 : 2 * Gm::G) + 256 + 32) * sizeof(float) +
+                        32 * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(encode_kernel<K, TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
@@ -752,7 +893,7 @@ exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
 
 exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
     switch (p.K) {
-    case 1: return launch_encode_k1(p, s, false);
+    case 1: return launch_k<1>(p, s, false);
     case 2: return launch_k<2>(p, s, false);
     case 3: return launch_k<3>(p, s, false);
     case 4: return launch_k<4>(p, s, false);
@@ -762,7 +903,7 @@ exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
 
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s) {
     switch (p.K) {
-    case 1: return launch_encode_k1(p, s, true);
+    case 1: return launch_k<1>(p, s, true);
     case 2: return launch_k<2>(p, s, true);
     case 3: return launch_k<3>(p, s, true);
     case 4: return launch_k<4>(p, s, true);

@@ -443,7 +443,7 @@ exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s) {
     ldlq_first_target_kernel<<<(unsigned)((16 * cols + 255) / 256), 256, 0, s>>>(p.R, cols,
                                                                                   16 * (B - 1), p.U);
     note_launch();
-    const int64_t need = TC * (p.K == 1 ? 2 : 1);
+    const int64_t need = TC;
     for (int64_t j = B - 1; j >= 0; j--) {
         EncodeLaunch el{};
         el.Y = p.U;

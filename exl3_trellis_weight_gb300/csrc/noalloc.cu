@@ -13,8 +13,7 @@
 // is loaded on a device and stays allocated on every device that loads the
 // library until the process exits.  Its host-side name is only a stand-in: the
 // device address is looked up with cudaGetSymbolAddress once per device (again
-// after that device's context was destroyed and re-created).  K = 1, whose
-// tiles run on two-block clusters, is not offered here.
+// after that device's context was destroyed and re-created).
 #include <mutex>
 
 #include "common.cuh"
@@ -124,8 +123,8 @@ extern "C" EXL3_API exl3_status exl3_encode_tiles_noalloc(const float *Y, int64_
     if (rows > (1ll << 24) || cols > (1ll << 24) || rows * cols > (1ll << 34))
         return set_error(EXL3_ERR_INVALID_ARG, "matrix %lldx%lld is too large", (long long)rows,
                          (long long)cols);
-    if (K < 2 || K > 4)
-        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d: the workspace-free encode takes K in {2,3,4}", K);
+    if (K < 1 || K > 4)
+        return set_error(EXL3_ERR_UNSUPPORTED, "K=%d is not built (K in {1,2,3,4})", K);
     if (!(scale > 0.0f) || !(scale < __builtin_inff()) || !(1.0f / scale < __builtin_inff()))
         return set_error(EXL3_ERR_INVALID_ARG, "scale and 1 / scale must be positive and finite");
     if (blocks < 0 || blocks > kNoAllocMaxBlocks)

@@ -318,7 +318,7 @@ exl3_status run_grid_search(const GridSearchLaunch &p, cudaStream_t s) {
         el.codes = p.codes_buf;
         el.tile_cost = nullptr;
         el.scratch = p.enc;
-        el.grid = p.grid < n_rows * (p.K == 1 ? 2 : 1) ? p.grid : n_rows * (p.K == 1 ? 2 : 1);
+        el.grid = p.grid < n_rows ? p.grid : n_rows;
         if ((e2 = launch_encode(el, s)) != EXL3_OK) return e2;
         row_error_kernel<<<n_rows, 256, 0, s>>>(p.codes_buf, p.K, p.R, p.cols, p.sample, n_slots,
                                                 stride, p.count, half_count, p.s_per_g, p.row_sum);

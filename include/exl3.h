@@ -125,9 +125,6 @@ EXL3_API size_t exl3_encode_workspace_min_bytes(int K);
  *   Y      (device) fp32 [rows, cols], the rotated matrix; targets are
  *          y = fl(Y * fl32(1/scale)).
  *   rows, cols: positive multiples of 16.   K in {1, 2, 3, 4}.   scale > 0, finite.
- *   K = 1 runs each tile on a cluster of two blocks (the 2^15-entry cost row is
- *   split between their shared memories), so its workspace holds an even
- *   number of block slices (minimum two).
  *   codes  (device, 4-byte aligned) uint16 [rows/16][cols/16][16*K].  For each
  *          tile the codes e_i (low K bits of the chosen state at element i)
  *          form the bitstream e_0 || e_1 || ... || e_255, each code MSB first.
@@ -377,10 +374,9 @@ EXL3_API exl3_status exl3_regularize(const void *W, int dt, int64_t rows, int64_
  * owns all device memory through its own pool, and latency-critical loops that
  * cannot afford an allocation (cudaMalloc may synchronise the whole device).
  *
- * Same inputs, outputs, layout and results as exl3_encode_tiles for K in
- * {2, 3, 4}; K = 1 (whose tiles run on two-block clusters) is not offered here
- * and returns EXL3_ERR_UNSUPPORTED.  The decision rows live in a static device
- * array inside the library instead of a caller workspace.  That array holds at
+ * Same inputs, outputs, layout and results as exl3_encode_tiles (K in
+ * {1, 2, 3, 4}).  The decision rows live in a static device array inside the
+ * library instead of a caller workspace.  That array holds at
  * most EXL3_NOALLOC_MAX_BLOCKS persistent blocks (8 blocks x 3,137,536 bytes,
  * about 24 MiB) and stays allocated on every device that loads the library's
  * device code until the process exits.
@@ -428,12 +424,11 @@ EXL3_API exl3_status exl3_profile_read(double *encode_ms, int64_t *encode_launch
                               int64_t *kernel_launches);
 
 /*
- * Device-side wait accounting (no counterpart on the pages).  Two kernels wait
- * on asynchronous arrivals: at K = 1 the two blocks of an encode cluster wait on
- * each other's pushed costs once per trellis step, and the forward rotation of
- * bf16 weights waits for its TMA tile loads.  Each such wait gives up after one
- * second, after which the block stops waiting for the rest of the launch and
- * that launch's results are void.  exl3_wait_timeouts synchronises the device,
+ * Device-side wait accounting (no counterpart on the pages).  One kernel waits
+ * on asynchronous arrivals: the forward rotation of bf16 weights waits for its
+ * TMA tile loads.  Each such wait gives up after one second, after which the
+ * block issues no further loads, waits (bounded) for the loads it already
+ * issued, and the launch's results are void.  exl3_wait_timeouts synchronises the device,
  * stores in *count_out (may be NULL) the number of expired waits since the
  * previous call and resets it; it returns EXL3_ERR_TIMEOUT when that number is
  * nonzero, EXL3_ERR_CUDA when the device could not be read, else EXL3_OK.  The

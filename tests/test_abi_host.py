@@ -70,7 +70,7 @@ def test_encode_rejects_bad_arguments(ex):
                                    a["cost"], a["ws"], a["ws_bytes"], a["stream"])
 
     assert call(K=0) == 2 and call(K=5) == 2               # unsupported K
-    assert call(K=1, ws_bytes=ws_min) == 3                 # K=1 needs two block slices
+    assert call(K=1, ws_bytes=ws_min - 256) == 3           # below one block slice
     assert call(rows=40) == 2 and call(cols=24) == 2       # not multiples of 16
     assert call(rows=0) == 1 and call(cols=-16) == 1
     assert call(Y=None) == 1 and call(codes=None) == 1
@@ -146,10 +146,10 @@ def test_ldl_and_ldlq_reject_bad_arguments(ex):
     assert lq(codes=None) == 1
     assert lq(w=64 * 128 * 4) == 3
     assert ex.ldlq_workspace_bytes(64, 128, 0) == 0
-    # K=1 needs two encode blocks (one cluster)
+    # every K needs at least one encode block slice on top of the fixed part
     w1 = ex.ldlq_workspace_bytes(64, 128, 1)
-    fixed = w1 - (w1 - 64 * 128 * 4) // ex.encode_workspace_min_bytes(2) * ex.encode_workspace_min_bytes(2)
-    assert lq(K=1, w=fixed + ex.encode_workspace_min_bytes(2)) == 3
+    fixed = w1 - (w1 - 64 * 128 * 4) // ex.encode_workspace_min_bytes(1) * ex.encode_workspace_min_bytes(1)
+    assert lq(K=1, w=fixed + ex.encode_workspace_min_bytes(1) - 256) == 3
 
 
 def test_regularize_rejects_bad_arguments(ex):
@@ -173,7 +173,7 @@ def test_workspace_queries_scale_with_work(ex):
     assert 0 < a <= b
     assert a == 10 * ex.encode_workspace_min_bytes(2)
     assert ex.encode_workspace_bytes(100, 0) == 0
-    assert ex.encode_workspace_min_bytes(1) == 2 * ex.encode_workspace_min_bytes(2)
+    assert all(ex.encode_workspace_min_bytes(k) == ex.encode_workspace_min_bytes(2) for k in (1, 3, 4))
     assert ex.quantize_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4
     assert ex.gss_workspace_bytes(4096, 4096, 2) > ex.quantize_workspace_bytes(4096, 4096, 2)
     assert ex.scale_search_workspace_bytes(4096, 4096, 2) > 4096 * 4096 * 4

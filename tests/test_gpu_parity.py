@@ -34,7 +34,7 @@ DEV = "cuda:0"
 
 @pytest.fixture(autouse=True)
 def _no_expired_waits(ex):
-    """No bounded device wait (the K=1 clusters') may give up in any test."""
+    """No bounded device wait (the TMA rotation's) may give up in any test."""
     yield
     assert ex.wait_timeouts() == 0
 
@@ -82,7 +82,7 @@ def test_encode_ragged_tiles_and_small_grids(ex, K, blocks):
     Y = rng.standard_normal((48, 80)).astype(np.float32) * 0.7
     ws = None
     if blocks is not None:
-        # the minimum workspace is one block slice (two, i.e. one cluster, at K=1)
+        # the minimum workspace is one block slice
         ws = torch.empty(blocks * ex.encode_workspace_min_bytes(K), dtype=torch.uint8, device=DEV)
     codes, cost = ex.encode_tiles(torch.from_numpy(Y).to(DEV), K, scale=0.7, want_cost=True, ws=ws)
     torch.cuda.synchronize()
@@ -368,7 +368,8 @@ def test_full_mlp12288_k4_sampled(ex):
 
 
 def test_full_linear4096_k1_sampled(ex):
-    """K=1 (two-block clusters) at full size, the bench's launch configuration."""
+    """K=1 (one block per tile, cost row updated in place) at full size, the bench's
+    launch configuration."""
     (_, W, su, sv, _), = inputs.workload("linear4096_k2")
     _check_full(ex, W, su, sv, 1, 24, 5)
 

@@ -57,6 +57,8 @@ def test_noalloc_matches_workspace_encode_on_consecutive_calls(lib):
     cases = [  # (rows, cols, K, scale, blocks, seed): second call reuses the static rows
         (128, 256, 2, 1.0, 0, 1),
         (96, 160, 4, 0.8, 3, 2),
+        (64, 96, 1, 1.1, 5, 3),
+        (48, 112, 3, 0.9, 0, 4),
     ]
     for rows, cols, K, scale, blocks, seed in cases:
         Yc = inputs.iid_f32(rows, cols, seed)
@@ -85,13 +87,12 @@ def test_noalloc_rejects_more_blocks_than_the_static_array_holds(lib):
     assert b"at most" in L.exl3_last_error()
 
 
-def test_noalloc_rejects_k1(lib):
-    """K = 1 tiles run on two-block clusters, which this entry point does not
-    offer: it returns EXL3_ERR_UNSUPPORTED and enqueues nothing."""
+def test_noalloc_rejects_an_unbuilt_k(lib):
+    """K outside {1, 2, 3, 4} returns EXL3_ERR_UNSUPPORTED and enqueues nothing."""
     _, L = lib
     Y = torch.zeros(16, 16, device="cuda:0")
-    codes = torch.full((1, 1, 16), 7, dtype=torch.int16, device="cuda:0")
-    st = L.exl3_encode_tiles_noalloc(ctypes.c_void_p(Y.data_ptr()), 16, 16, 1, ctypes.c_float(1.0),
+    codes = torch.full((1, 1, 80), 7, dtype=torch.int16, device="cuda:0")
+    st = L.exl3_encode_tiles_noalloc(ctypes.c_void_p(Y.data_ptr()), 16, 16, 5, ctypes.c_float(1.0),
                                      ctypes.c_void_p(codes.data_ptr()), None, 0, None)
     assert st == 2   # EXL3_ERR_UNSUPPORTED
     torch.cuda.synchronize()
