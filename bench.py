@@ -63,9 +63,10 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu + encode_common.cuh + common.cuh -> DRAM bytes (read +
     # write) per tile at K=2, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
-    # on 1,216 tiles of N(0, 1) targets (profile case `encode`); the traffic is the
-    # decision rows, proportional to the tiles processed.
-    "c71e4a2c30ece1f527139dc0395d9ec75186e3f5dbc44cd97d129636961db727": 1545464.0,
+    # on 1,216 tiles of N(0, 1) targets (bench.py --case encode --K 2 --rows 1216
+    # --cols 256): 31.93 MB + 1.8495 GB; the traffic is the decision rows,
+    # proportional to the tiles processed.
+    "0bd58932d6ed4d4a1aef03b75456eb46ddb8798e41e4bf7a77a9743ff4bd190a": 1547240.0,
 }
 
 WORKLOAD = "linear4096_k2"
