@@ -217,6 +217,24 @@ __host__ __device__ __forceinline__ uint32_t rotr15(uint32_t x, int s) {
 }
 __host__ __device__ __forceinline__ uint32_t k1_pad(uint32_t p) { return p + (p >> 5) + (p >> 10); }
 
+// per-step values of acs_step_k1 for s = 0..14: the five Gray-walk steps
+// k1_pad(rotr^s(2^(9+b))) and the k = 1 offset k1_pad(rotr^s(2^14))
+struct K1Tab {
+    uint32_t v[15][6];
+};
+constexpr K1Tab k1_make_tab() {
+    K1Tab t{};
+    for (int s = 0; s < 15; s++) {
+        for (int b = 0; b < 6; b++) {
+            const uint32_t x = 1u << (9 + b);
+            const uint32_t r = ((x >> s) | (x << (15 - s))) & 0x7FFFu;
+            t.v[s][b] = r + (r >> 5) + (r >> 10);
+        }
+    }
+    return t;
+}
+__constant__ K1Tab k1_tab = k1_make_tab();
+
 // D_t(g) of entry g (15 bits): thread h & 511 of unit h = g >> 1, word i >> 4,
 // bit 2 (i & 15) + (g & 1), with i = h >> 9
 __host__ __device__ __forceinline__ void k1_dec_locate(uint32_t g, int &word, int &bit) {
@@ -241,10 +259,8 @@ __device__ __forceinline__ void acs_step_k1(float *M, const float y, const uint3
     constexpr int BATCH = 4;
     word[0] = 0u;
     word[1] = 0u;
-    const uint32_t E0 = k1_pad(rotr15(1u << 9, s)), E1 = k1_pad(rotr15(1u << 10, s)),
-                   E2 = k1_pad(rotr15(1u << 11, s)), E3 = k1_pad(rotr15(1u << 12, s)),
-                   E4 = k1_pad(rotr15(1u << 13, s));
-    const uint32_t D = k1_pad(rotr15(1u << 14, s));
+    const uint32_t E0 = k1_tab.v[s][0], E1 = k1_tab.v[s][1], E2 = k1_tab.v[s][2],
+                   E3 = k1_tab.v[s][3], E4 = k1_tab.v[s][4], D = k1_tab.v[s][5];
     uint32_t a0 = k1_pad(rotr15((uint32_t)tid, s));
     // every position is read, then rewritten, by the one unit that owns it at
     // this step, and different units' positions never coincide: loads go
