@@ -23,8 +23,14 @@
 // buffer, 64 KiB output stage.
 //
 // Each wait for a TMA load is bounded in time: on expiry the block stops
-// waiting, its results are void, and a device counter records it (read with
-// the K=1 encoder's count by exl3_wait_timeouts).
+// waiting, issues no further load, waits (bounded) for the loads it issued,
+// its results are void, and a device counter records it (exl3_wait_timeouts).
+//
+// The kernel is launched with programmatic stream serialization: its prologue
+// (barrier set-up) may overlap the tail of the previous kernel in the stream,
+// `griddepcontrol.wait` holds every global access until that kernel has
+// completed, and each block allows the next kernel to launch once it has
+// started its last 128 x 128 block (4096 x 4096: 25.0 -> 22.4 us).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -148,6 +154,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // before the next one on the same stage is issued, so at most one is in
     // flight per stage and each barrier is at most one phase behind)
     int issued0 = 0, issued1 = 0;
+    // programmatic dependent launch: everything above overlaps the previous
+    // kernel's tail; global memory is read only after it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (t == 0 && (int)blockIdx.x < nblk) {
         issue_load(&in_map, su, sv, base, bar0, (int)blockIdx.x, nbc);
         issued0 = 1;
@@ -169,6 +178,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 issued1++;
         }
         bar_wait(bar0 + 8u * (uint32_t)st, (uint32_t)(it >> 1) & 1u, &gave_up);
+        // the last block of this CTA: the next kernel in the stream may start its prologue
+        if (blk + (int)gridDim.x >= nblk)
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
         // ---- phase 1: row i, columns 32 jh .. 32 jh + 31 -> j spans 1..16 -------
         {
@@ -362,8 +374,22 @@ exl3_status launch_rotate_fwd_tma(const RotateLaunch &p, cudaStream_t s) {
     if (e != cudaSuccess)
         return cuda_check(e, "cudaFuncSetAttribute(rotate_fwd_tma)");
     const int64_t grid = nblk < device_sm_count() ? nblk : device_sm_count();
-    rotate_fwd_tma_kernel<<<(unsigned)grid, kTmaThreads, smem, s>>>(in_map, out_map, p.su, p.sv, (int)p.rows,
-                                                                     (int)p.cols, p.tile_sums);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float *su_ = p.su, *sv_ = p.sv;
+    int rows_ = (int)p.rows, cols_ = (int)p.cols;
+    double *ts_ = p.tile_sums;
+    e = cudaLaunchKernelEx(&cfg, rotate_fwd_tma_kernel, in_map, out_map, su_, sv_, rows_, cols_, ts_);
+    if (e != cudaSuccess)
+        return cuda_check(e, "rotate_fwd_tma launch");
     note_launch();
     note_rotate_kernel(1);
     return cuda_check(cudaGetLastError(), "rotate_fwd_tma launch");
