@@ -657,7 +657,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
     uint32_t *bsb = reinterpret_cast<uint32_t *>(ysb + 512);       // [x][32]
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bsb + 64);   // [32]
     __shared__ uint32_t sh_sstar[2][2], sh_end[2][2];             // [unit slot][x]
+    // this thread's traceback (threads 0 and 32 only): registers at K = 4 (1.7 %
+    // faster), shared memory at K = 3 (2.5 % slower in registers)
     __shared__ Tb2 tbs[2];
+    Tb2 tb_local;
 
     const int tid = threadIdx.x;
     const int my_tb = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
@@ -690,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
     uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
 
     if (my_tb >= 0) {
-        Tb2 &tb = tbs[my_tb];
+        Tb2 &tb = K == 4 ? tb_local : tbs[my_tb & 1];
         tb.on = false;
         tb.rows = nullptr;
         tb.tile = 0;
@@ -756,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
         }
         const bool has_b1 = b_loc >= 0 && 2 * b_loc + 1 < n_my;
         if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
-            Tb2 &tb = tbs[my_tb];
+            Tb2 &tb = K == 4 ? tb_local : tbs[my_tb & 1];
             uint32_t *bs = bsb + 32 * my_tb;
             tb.on = true;
             tb.pass = b_pass;
@@ -785,8 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
             float *const A0 = Mb, *const A1 = Mb + Gm::G;             // tile 0 buffers
             float *const B0 = Mb + 2 * Gm::G, *const B1 = Mb + 3 * Gm::G;   // tile 1 buffers
             for (int t = 0; t < T - 1; t++) {
-                if (my_tb >= 0 && tbs[my_tb].on)
-                    tb2_issue<K>(tbs[my_tb]);
+                if (my_tb >= 0 && (K == 4 ? tb_local : tbs[my_tb & 1]).on)
+                    tb2_issue<K>(K == 4 ? tb_local : tbs[my_tb & 1]);
                 uint32_t word[Gm::DW];
                 unsigned long long key = 0ull;
                 acs_step<K, false>((t & 1) ? A1 : A0, (t & 1) ? A0 : A1, ysb[t], vpk, tid, word, key);
@@ -798,21 +801,21 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
                     if (t >= row0)
                         dual_store_row<K>(rows1 + (size_t)(t - row0) * Du::RW, word1, tid);
                 }
-                if (my_tb >= 0 && tbs[my_tb].on)
-                    tb2_advance<K>(tbs[my_tb], bsb + 32 * my_tb);
+                if (my_tb >= 0 && (K == 4 ? tb_local : tbs[my_tb & 1]).on)
+                    tb2_advance<K>(K == 4 ? tb_local : tbs[my_tb & 1], bsb + 32 * my_tb);
                 __syncthreads();
             }
             if (f_pass == 1) {
                 // step T-1: lowest full state with minimal cost, per tile
-                if (my_tb >= 0 && tbs[my_tb].on)
-                    tb2_issue<K>(tbs[my_tb]);
+                if (my_tb >= 0 && (K == 4 ? tb_local : tbs[my_tb & 1]).on)
+                    tb2_issue<K>(K == 4 ? tb_local : tbs[my_tb & 1]);
                 uint32_t word[Gm::DW];
                 unsigned long long key0 = ~0ull, key1 = ~0ull;
                 acs_step<K, true>(A1, nullptr, ysb[T - 1], vpk, tid, word, key0);
                 if (has1)
                     acs_step<K, true>(B1, nullptr, ysb[256 + T - 1], vpk, tid, word, key1);
-                if (my_tb >= 0 && tbs[my_tb].on)
-                    tb2_advance<K>(tbs[my_tb], bsb + 32 * my_tb);
+                if (my_tb >= 0 && (K == 4 ? tb_local : tbs[my_tb & 1]).on)
+                    tb2_advance<K>(K == 4 ? tb_local : tbs[my_tb & 1], bsb + 32 * my_tb);
                 key0 = warp_min_u64(key0);
                 key1 = warp_min_u64(key1);
                 if ((tid & 31) == 0) {
@@ -841,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
             }
         }
         if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
-            Tb2 &tb = tbs[my_tb];
+            Tb2 &tb = K == 4 ? tb_local : tbs[my_tb & 1];
             uint32_t *bs = bsb + 32 * my_tb;
             while (tb.on) {
                 tb2_issue<K>(tb);
