@@ -1,5 +1,4 @@
-// encode_common.cuh -- device helpers shared by the trellis encode kernels
-// (encode.cu: one block per tile; encode_k1.cu: a two-block cluster per tile).
+// encode_common.cuh -- device helpers of the trellis encode kernels (encode.cu).
 #pragma once
 
 #include "common.cuh"
@@ -28,23 +27,6 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
         v = w < v ? w : v;
     }
     return v;
-}
-
-// fl(fl(v - y)^2) for the two fp16 levels packed in vw, as one 64-bit pair: the
-// two mixed-precision subtracts (exact widening of v, one binary32 rounding;
-// (v - y)^2 == (y - v)^2 bitwise) write the halves of the 64-bit operand of one
-// f32x2 multiply.  The K=1 encoder adds the costs with scalar adds (the packed
-// form below measured 0.8 % slower there).
-__device__ __forceinline__ unsigned long long sq_pair(const uint32_t vw, const float y) {
-    unsigned long long q;
-    asm("{\n\t.reg .b16 hl, hh;\n\t.reg .f32 a, b;\n\t.reg .b64 d;\n\t"
-        "mov.b32 {hl, hh}, %1;\n\t"
-        "sub.rn.f32.f16 a, hl, %2;\n\t"
-        "sub.rn.f32.f16 b, hh, %2;\n\t"
-        "mov.b64 d, {a, b};\n\t"
-        "mul.rn.f32x2 %0, d, d;\n\t}"
-        : "=l"(q) : "r"(vw), "f"(y));
-    return q;
 }
 
 // Two candidates: fl(m + fl(fl(v - y)^2)) for the two fp16 levels packed in vw
