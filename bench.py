@@ -546,8 +546,10 @@ def run_ours(args):
         aux["block_ldl"] = {"n": rows, "ms": sum(ldl_ms) / len(ldl_ms), "retries": retries,
                             "hessian": "spd_hessian(4096, seed 50, rho 0.95): AR(1) channels, "
                                        "lognormal channel scales, 8192 rows, 1% damping"}
+        sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
         aux["ldlq"] = {"ms": lq_avg, "tiles_per_s": n_tiles / (lq_avg / 1e3),
                        "spans": rows // 16, "tiles_per_span": cols // 16,
+                       "tiles_per_launch": min(sm_count * (2 if K >= 3 else 1), cols // 16),
                        "encode_share": (lq_enc_ms / len(lq_ms)) / lq_avg,
                        "encode_launches": lq_enc_n // len(lq_ms)}
         del ws_q, codes_q, R

@@ -809,8 +809,9 @@ static size_t ldlq_carve(void *ws, int64_t rows, int64_t cols, int grid, LdlqLau
     Carver c(ws);
     LdlqLaunch l{};
     l.acc = (float *)c.take((size_t)rows * cols * sizeof(float));
-    l.U = (float *)c.take((size_t)16 * cols * sizeof(float));
-    l.E = (float *)c.take((size_t)16 * cols * sizeof(float));
+    l.U = (float *)c.take((size_t)32 * cols * sizeof(float));          // two span rows
+    l.E = (float *)c.take((size_t)16 * cols * sizeof(float));          // cols / 16 tiles
+    l.ring = (uint32_t *)c.take((size_t)2 * (cols / 16) * 32 * sizeof(uint32_t));   // K <= 4
     l.enc = (uint32_t *)c.take((size_t)grid * kEncodeBlockScratchBytes);
     l.grid = grid;
     if (out)

@@ -165,6 +165,12 @@ struct EncodeLaunch {
     float *tile_cost;            // nullable
     uint32_t *scratch;           // grid * kEncodeBlockScratchBytes
     int grid;
+    // tiles coded: n_work tiles (0: all) from tile tile0 on; with ring > 0 the
+    // tile index wraps at ring (the matrix's tile count); codes and costs go to
+    // the tiles' own positions
+    int tile0;
+    int n_work;
+    int ring;
 };
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s);
 // same launch without the profiling hooks (creates no CUDA events)
@@ -256,7 +262,9 @@ struct LdlqLaunch {
     uint32_t *codes;        // [rows/16, cols/16, 8K words]
     float *Q;               // nullable [rows, cols]
     float *acc;             // [rows, cols]
-    float *U, *E;           // [16, cols] each
+    float *U;               // [2][16, cols]: targets of two span rows (a ring)
+    float *E;               // [cols / 16][256]: errors of one launch's tiles
+    uint32_t *ring;         // [2][cols / 16][8K words]: codes of two span rows
     uint32_t *enc;          // encode scratch, grid blocks
     int grid;
 };

@@ -317,6 +317,15 @@ __device__ __forceinline__ void acs_step_k1(float *M, const float y, const uint3
     }
 }
 
+// Matrix tile of a block's l-th tile: the launch's tiles tile0, tile0 + 1, ...
+// (wrapping at a.ring when that is set) are dealt to the blocks round-robin.  It
+// reads only launch parameters, so nothing extra stays live through the forward
+// loop (a wrap against a kept tile count cost 2.6 % at K=2).
+__device__ __forceinline__ int tile_at(const EncodeLaunch &a, const int l, const int grid) {
+    const int t = a.tile0 + (int)blockIdx.x + l * grid;
+    return (a.ring > 0 && t >= a.ring) ? t - a.ring : t;
+}
+
 template <int K>
 __device__ __forceinline__ void tb_issue(Tb &tb) {
     int w, b;
@@ -339,6 +348,65 @@ __device__ __forceinline__ void tb_advance(Tb &tb, uint32_t *bs) {
         tb.on = false;
 }
 
+// ---------------------------------------------------------------------------
+// A traceback with no forward pass beside it (a block's last tile, or launches
+// of one tile per block, as in LDLQ) would expose its chain of dependent L2
+// loads, about 0.4 us a step.  There warp 0 streams the decision rows t-1,
+// t-2, ... into shared memory kTbAhead rows ahead (cp.async, 16 bytes a lane
+// per copy, one commit group per row; the rows do not depend on the path) and
+// lane 0 walks the chain from shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kTbAhead = 16;
+constexpr size_t kTbStreamBytes = (size_t)kTbAhead * kRowWords * sizeof(uint32_t);
+
+__device__ __forceinline__ void tb_copy_row(uint32_t *dst, const uint32_t *src, const int lane) {
+#pragma unroll
+    for (int i = 0; i < kRowWords / 128; i++) {       // 8 x 16 bytes per lane
+        const int c = (lane + 32 * i) * 4;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                     ::"r"((uint32_t)__cvta_generic_to_shared(dst + c)), "l"(src + c) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Called by all of warp 0; the traceback state is lane 0's.  Out of line: inlined
+// into the kernel, its code changed the forward loop's and cost it 17 % at K=2.
+template <int K>
+__device__ __noinline__ Tb tb_drain_streamed(Tb tb, uint32_t *bs, uint32_t *pf, const int lane) {
+    const unsigned long long rp = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)tb.rows, 0);
+    const int t0 = __shfl_sync(0xffffffffu, tb.t, 0);
+    const int n = t0 - __shfl_sync(0xffffffffu, tb.stop, 0);
+    const int row0 = __shfl_sync(0xffffffffu, tb.row0, 0);
+    // the row of the q-th step back is first - q rows
+    const uint32_t *first = reinterpret_cast<const uint32_t *>((uintptr_t)rp) + (size_t)(t0 - 1 - row0) * kRowWords;
+#pragma unroll 1
+    for (int q = 0; q < kTbAhead; q++) {
+        if (q < n)
+            tb_copy_row(pf + q * kRowWords, first - (size_t)q * kRowWords, lane);
+        cp_async_commit();
+    }
+#pragma unroll 1
+    for (int q = 0; q < n; q++) {
+        cp_async_wait<kTbAhead - 1>();      // this lane's copies of row q have landed
+        __syncwarp();                       // and every lane's
+        if (lane == 0) {
+            int w, b;
+            dec_loc<K>(tb.s >> K, w, b);
+            tb.pending = pf[(q % kTbAhead) * kRowWords + w];
+            tb_advance<K>(tb, bs);
+        }
+        __syncwarp();                       // the slot is read before it is refilled
+        if (q + kTbAhead < n)
+            tb_copy_row(pf + (q % kTbAhead) * kRowWords, first - (size_t)(q + kTbAhead) * kRowWords, lane);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    return tb;
+}
+
 // TT: tile length fixed at compile time (256 for 16x16 tiles) or 0 (rows of
 // a.T targets).
 template <int K, int TT>
@@ -351,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     float *ys = K == 1 ? M0 + kK1RowFloats + 2 : M1 + Gm::G;     // up to 256 targets
     uint32_t *bs = reinterpret_cast<uint32_t *>(ys + 256);         // packed codes (tb2)
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bs + 32);
+    uint32_t *pf = reinterpret_cast<uint32_t *>(red + 32);          // kTbAhead streamed rows
     __shared__ uint32_t sh_sstar[2], sh_end[2];
     // traceback state, used by thread 0 only: registers at K = 1 (1.7 % faster),
     // shared memory at K = 2 (in registers it spilled and ran 4 % slower)
@@ -396,8 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
     const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
     const int grid = (int)gridDim.x;
     // a non-finite inverse scale (a rejected weight, see scale_kernel) codes no tile
-    const int n_my = (isfinite(inv_s) && n_tiles > (int)blockIdx.x)
-                         ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
+    const int n_work = a.n_work > 0 ? a.n_work : n_tiles;
+    const int n_my = (isfinite(inv_s) && n_work > (int)blockIdx.x)
+                         ? (n_work - (int)blockIdx.x + grid - 1) / grid : 0;
     // decision buffers of this block: pass-1 slots 0/1, then pass-2 slots 0/1
     uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
     constexpr size_t kP1 = (size_t)kRowsPass1 * kRowWords, kP2 = (size_t)kRowsPass2 * kRowWords;
@@ -436,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
             b_slot = 1; b_pass = 2; b_loc = 2 * p - 1;   // drain: last B's traceback
         }
         const bool fwd = f_loc >= 0;
-        const int f_tile = (int)blockIdx.x + f_loc * grid;
+        const int f_tile = tile_at(a, f_loc, grid);
 
         if (fwd) {
             if (tid < T) {
@@ -471,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
             tb.on = true;
             tb.pass = b_pass;
             tb.slot = b_slot;
-            tb.tile = (int)blockIdx.x + b_loc * grid;
+            tb.tile = tile_at(a, b_loc, grid);
             tb.t = T - 1;
             if (b_pass == 1) {
                 tb.s = sh_sstar[b_slot];
@@ -542,6 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncodeLaunch 
                 const float mprev = K == 1 ? M0[k1_pad(rotr15(e >> 1, (T - 1) % 15))] : M1[e >> K];
                 a.tile_cost[f_tile] = __fadd_rn(mprev, __fmul_rn(d, d));
             }
+        }
+        if (b_loc >= 0 && !fwd && tid < 32) {
+            const Tb r = tb_drain_streamed<K>(tb, bs, pf, tid);
+            if (tid == 0)
+                tb = r;
         }
         if (tid == 0 && b_loc >= 0) {
             while (tb.on) {
@@ -687,8 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
     const int tiles_c = row_tiles ? 1 : (int)(a.cols / 16);
     const int n_tiles = row_tiles ? (int)a.rows : (int)(a.rows / 16) * tiles_c;
     const int grid = (int)gridDim.x;
-    const int n_my = (isfinite(inv_s) && n_tiles > (int)blockIdx.x)
-                         ? (n_tiles - (int)blockIdx.x + grid - 1) / grid : 0;
+    const int n_work = a.n_work > 0 ? a.n_work : n_tiles;
+    const int n_my = (isfinite(inv_s) && n_work > (int)blockIdx.x)
+                         ? (n_work - (int)blockIdx.x + grid - 1) / grid : 0;
     const int n_units = (n_my + 1) / 2;                  // pairs of tiles
     uint32_t *const scr = a.scratch + (size_t)blockIdx.x * (kEncodeBlockScratchBytes / sizeof(uint32_t));
 
@@ -733,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
 
         if (fwd) {
             for (int x = 0; x < (has1 ? 2 : 1); x++) {
-                const int f_tile = (int)blockIdx.x + (2 * f_loc + x) * grid;
+                const int f_tile = tile_at(a, 2 * f_loc + x, grid);
                 float *ys = ysb + 256 * x;
                 if (tid < T) {
                     const int i = (f_pass == 1) ? (tid + half < T ? tid + half : tid + half - T) : tid;
@@ -763,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
             uint32_t *bs = bsb + 32 * my_tb;
             tb.on = true;
             tb.pass = b_pass;
-            tb.tile = (int)blockIdx.x + (2 * b_loc + my_tb) * grid;
+            tb.tile = tile_at(a, 2 * b_loc + my_tb, grid);
             tb.t = T - 1;
             tb.rows = scr + (size_t)(2 * b_slot + my_tb) * Du::SLOT;
             if (b_pass == 1) {
@@ -840,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
                 const uint32_t e = sh_end[f_slot][x];
                 const float d = __fsub_rn(ysb[256 * x + T - 1], mul1_value(e));
                 const float *M1x = x ? B1 : A1;
-                a.tile_cost[(int)blockIdx.x + (2 * f_loc + x) * grid] = __fadd_rn(M1x[e >> K], __fmul_rn(d, d));
+                a.tile_cost[tile_at(a, 2 * f_loc + x, grid)] = __fadd_rn(M1x[e >> K], __fmul_rn(d, d));
             }
         }
         if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
@@ -884,7 +960,7 @@ template <int K, int TT>
 exl3_status launch_kt(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
     const size_t smem = (size_t)((K == 1 ? kK1RowFloats + 2 : 2 * Gm::G) + 256 + 32) * sizeof(float) +
-                        32 * sizeof(unsigned long long);
+                        32 * sizeof(unsigned long long) + kTbStreamBytes;
     cudaError_t e = cudaFuncSetAttribute(encode_kernel<K, TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
@@ -914,7 +990,20 @@ exl3_status launch_k(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
 
 }  // namespace
 
+static exl3_status check_work(const EncodeLaunch &p) {
+    const int64_t n_tiles = p.row_tiles ? p.rows : (p.rows / 16) * (p.cols / 16);
+    const int64_t work = p.n_work > 0 ? p.n_work : n_tiles;
+    const bool ok = p.tile0 >= 0 && p.n_work >= 0 && work <= n_tiles &&
+                    (p.ring == 0 ? p.tile0 + work <= n_tiles : (p.ring == n_tiles && p.tile0 < n_tiles));
+    if (!ok)
+        return set_error(EXL3_ERR_INVALID_ARG, "tile range %d + %d (ring %d) outside %lld tiles",
+                         p.tile0, p.n_work, p.ring, (long long)n_tiles);
+    return EXL3_OK;
+}
+
 exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
+    if (exl3_status st = check_work(p); st != EXL3_OK)
+        return st;
     switch (p.K) {
     case 1: return launch_k<1>(p, s, false);
     case 2: return launch_k<2>(p, s, false);
@@ -925,6 +1014,8 @@ exl3_status launch_encode_unprofiled(const EncodeLaunch &p, cudaStream_t s) {
 }
 
 exl3_status launch_encode(const EncodeLaunch &p, cudaStream_t s) {
+    if (exl3_status st = check_work(p); st != EXL3_OK)
+        return st;
     switch (p.K) {
     case 1: return launch_k<1>(p, s, true);
     case 2: return launch_k<2>(p, s, true);

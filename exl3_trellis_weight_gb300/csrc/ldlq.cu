@@ -26,7 +26,7 @@ namespace exl3 {
 namespace {
 
 constexpr int kUpdTile = 64;     // trailing-update tile (64 x 64 entries, 4 x 4 per thread)
-constexpr int kFbRows = 32;      // rows per feedback block
+constexpr int kFbRows = 256;     // rows per feedback block
 
 // delta = (2 sigma_reg) * (sum of the diagonal, ascending / n)
 __global__ void __launch_bounds__(1024) diag_delta_kernel(const double *__restrict__ H, int64_t n,
@@ -253,52 +253,75 @@ __global__ void ldlq_first_target_kernel(const float *__restrict__ R, int64_t co
         U[e] = __fadd_rn(R[row0 * cols + e], 0.0f);
 }
 
-// one block (256 threads) per tile of the span at rows row0 .. row0+15:
-// q = fl32(v(state) * s), E = fl32(R - q); Q optional
-__global__ void __launch_bounds__(256) ldlq_error_kernel(const uint32_t *__restrict__ codes, int K,
+// Tiles in coding order: position p = sigma * TC + c is tile column c of span
+// j = B - 1 - sigma (spans bottom-up); its targets and codes sit in ring slot
+// sigma & 1 (ring tile p mod 2 TC).
+struct SpanTile {
+    int64_t j, c, slot;
+    __device__ SpanTile(int64_t p, int64_t TC, int64_t B) {
+        const int64_t sigma = p / TC;
+        j = B - 1 - sigma;
+        c = p - sigma * TC;
+        slot = sigma & 1;
+    }
+};
+
+// one block (256 threads) per tile coded by the launch (tiles p0 + blockIdx.x):
+// the codes move from the ring to their place, q = fl32(v(state) * s),
+// E = fl32(R - q); Q optional
+__global__ void __launch_bounds__(256) ldlq_error_kernel(const uint32_t *__restrict__ ring,
+                                                         uint32_t *__restrict__ codes, int K,
                                                          const float *__restrict__ R, int64_t cols,
-                                                         int64_t row0, float s, float *__restrict__ E,
-                                                         float *__restrict__ Q) {
+                                                         int64_t TC, int64_t B, int64_t p0, float s,
+                                                         float *__restrict__ E, float *__restrict__ Q) {
     __shared__ uint32_t cw[32];
-    const int64_t tile = blockIdx.x;
+    const SpanTile tl(p0 + blockIdx.x, TC, B);
     const int NW = 8 * K;
-    if (threadIdx.x < NW)
-        cw[threadIdx.x] = codes[tile * NW + threadIdx.x];
+    if (threadIdx.x < NW) {
+        const uint32_t w = ring[(tl.slot * TC + tl.c) * NW + threadIdx.x];
+        cw[threadIdx.x] = w;
+        codes[(tl.j * TC + tl.c) * NW + threadIdx.x] = w;
+    }
     __syncthreads();
     const int i = threadIdx.x;
-    const int64_t r = i >> 4, c = tile * 16 + (i & 15);
+    const int64_t r = 16 * tl.j + (i >> 4), c = 16 * tl.c + (i & 15);
     const float q = __fmul_rn(mul1_value(window_state_k(cw, i, K)), s);
-    E[r * cols + c] = __fsub_rn(R[(row0 + r) * cols + c], q);
+    E[(int64_t)blockIdx.x * 256 + i] = __fsub_rn(R[r * cols + c], q);
     if (Q)
-        Q[(row0 + r) * cols + c] = q;
+        Q[r * cols + c] = q;
 }
 
-// after span j: rows r < 16 j, acc = fmaf(M[i][r], E[i - 16j][c], acc) for
-// i = 16j+15 down to 16j; the rows of span j-1 get their targets
-// U = fl32(R + acc) (their accumulator is not needed any more)
+// after tile (j, c) is coded: rows r < 16 j of its 16 columns get
+// acc = fmaf(M[i][r], E[i - 16j][x], acc) for i = 16j+15 down to 16j; the rows
+// of span j-1 get their targets U = fl32(R + acc) in the next ring slot (their
+// accumulator is not needed any more).  Block (tile, 256-row chunk); thread =
+// (column x, row lane): rows chunk + lane + 16 k.
 __global__ void __launch_bounds__(256) ldlq_feedback_kernel(float *__restrict__ ACC,
                                                             const float *__restrict__ M, int64_t n,
-                                                            int64_t cols, int64_t j,
-                                                            const float *__restrict__ E,
+                                                            int64_t cols, int64_t TC, int64_t B,
+                                                            int64_t p0, const float *__restrict__ E,
                                                             const float *__restrict__ R,
                                                             float *__restrict__ U) {
     __shared__ float Ms[16][kFbRows];
-    const int64_t above = 16 * j;
+    const SpanTile tl(p0 + blockIdx.x, TC, B);
+    const int64_t above = 16 * tl.j;
     const int64_t r0 = (int64_t)blockIdx.y * kFbRows;
+    if (r0 >= above)
+        return;
     for (int e = threadIdx.x; e < 16 * kFbRows; e += blockDim.x) {
         const int ii = e / kFbRows, rr = e % kFbRows;
         Ms[ii][rr] = (r0 + rr < above) ? M[(above + ii) * n + r0 + rr] : 0.0f;
     }
-    __syncthreads();
-    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= cols)
-        return;
+    const int x = threadIdx.x & 15, lane = threadIdx.x >> 4;
     float e[16];
 #pragma unroll
     for (int ii = 0; ii < 16; ii++)
-        e[ii] = E[ii * cols + c];
+        e[ii] = E[(int64_t)blockIdx.x * 256 + ii * 16 + x];
+    __syncthreads();
+    const int64_t c = 16 * tl.c + x;
     const int64_t span_lo = above - 16;
-    for (int rr = 0; rr < kFbRows; rr++) {
+    float *const Un = U + (1 - tl.slot) * 16 * cols;
+    for (int rr = lane; rr < kFbRows; rr += 16) {
         const int64_t r = r0 + rr;
         if (r >= above)
             break;
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(256) ldlq_feedback_kernel(float *__restrict__ 
         for (int ii = 15; ii >= 0; ii--)
             a = __fmaf_rn(Ms[ii][rr], e[ii], a);
         if (r >= span_lo)
-            U[(r - span_lo) * cols + c] = __fadd_rn(R[r * cols + c], a);
+            Un[(r - span_lo) * cols + c] = __fadd_rn(R[r * cols + c], a);
         else
             ACC[r * cols + c] = a;
     }
@@ -434,8 +457,15 @@ exl3_status run_block_ldl(const BlockLdlLaunch &p, cudaStream_t s) {
 exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s) {
     const int64_t n = p.rows, cols = p.cols;
     const int64_t B = n / 16, TC = cols / 16;
-    const int64_t words = 8 * (int64_t)p.K;          // uint32 words per tile
     const float inv = 1.0f / p.scale;
+    // Tile (j, c) depends only on the tiles below it in column c, so the tiles
+    // are coded in span-major order, bottom-up, one round of the persistent grid
+    // per launch (K >= 3: a pair per block) and at most one span row (TC tiles)
+    // per launch: a tile's nearest dependency, TC positions back, then always
+    // lies in an earlier launch, whose feedback has written its targets.
+    const int64_t round = (int64_t)p.grid * (p.K >= 3 ? 2 : 1);
+    const int64_t G = round < TC ? round : TC;
+    const int64_t total = B * TC;
     exl3_status st;
     if ((st = cuda_check(cudaMemsetAsync(p.acc, 0, (size_t)n * cols * sizeof(float), s),
                          "feedback clear")) != EXL3_OK)
@@ -443,28 +473,32 @@ exl3_status run_ldlq(const LdlqLaunch &p, cudaStream_t s) {
     ldlq_first_target_kernel<<<(unsigned)((16 * cols + 255) / 256), 256, 0, s>>>(p.R, cols,
                                                                                   16 * (B - 1), p.U);
     note_launch();
-    const int64_t need = TC;
-    for (int64_t j = B - 1; j >= 0; j--) {
+    for (int64_t p0 = 0; p0 < total; p0 += G) {
+        const int64_t cnt = total - p0 < G ? total - p0 : G;
         EncodeLaunch el{};
-        el.Y = p.U;
-        el.rows = 16;
+        el.Y = p.U;                  // the ring: 2 span rows of targets
+        el.rows = 32;
         el.cols = cols;
         el.K = p.K;
         el.T = 256;
         el.row_tiles = 0;
         el.inv_scale = inv;
         el.inv_scale_dev = nullptr;
-        el.codes = p.codes + j * TC * words;
+        el.codes = p.ring;
         el.tile_cost = nullptr;
         el.scratch = p.enc;
-        el.grid = (int)(p.grid < need ? p.grid : need);
+        el.grid = (int)(p.grid < cnt ? p.grid : cnt);
+        el.tile0 = (int)(p0 % (2 * TC));
+        el.n_work = (int)cnt;
+        el.ring = (int)(2 * TC);
         if ((st = launch_encode(el, s)) != EXL3_OK) return st;
-        ldlq_error_kernel<<<(unsigned)TC, 256, 0, s>>>(p.codes + j * TC * words, p.K, p.R, cols,
-                                                        16 * j, p.scale, p.E, p.Q);
+        ldlq_error_kernel<<<(unsigned)cnt, 256, 0, s>>>(p.ring, p.codes, p.K, p.R, cols, TC, B, p0,
+                                                        p.scale, p.E, p.Q);
         note_launch();
-        if (j > 0) {
-            const dim3 g((unsigned)((cols + 255) / 256), (unsigned)((16 * j + kFbRows - 1) / kFbRows));
-            ldlq_feedback_kernel<<<g, 256, 0, s>>>(p.acc, p.M, n, cols, j, p.E, p.R, p.U);
+        const int64_t j_top = B - 1 - p0 / TC;       // the launch's highest span
+        if (j_top > 0) {
+            const dim3 g((unsigned)cnt, (unsigned)((16 * j_top + kFbRows - 1) / kFbRows));
+            ldlq_feedback_kernel<<<g, 256, 0, s>>>(p.acc, p.M, n, cols, TC, B, p0, p.E, p.R, p.U);
             note_launch();
         }
         if ((st = cuda_check(cudaGetLastError(), "ldlq launch")) != EXL3_OK) return st;

@@ -321,8 +321,10 @@ EXL3_API exl3_status exl3_block_ldl(const double *H, int64_t n, double sigma_reg
  *     reconstruction fl32(v * scale) of every span.
  *   ws: exl3_ldlq_workspace_bytes(rows, cols, K); a smaller workspace (at least
  *     the K's encode minimum on top of the fixed part) runs fewer encode blocks.
- * The spans are coded one after another (each depends on the errors of the
- * ones below it): rows / 16 encode launches of cols / 16 tiles each.
+ * A tile depends on the errors of the tiles below it in its own tile column,
+ * so the tiles are coded bottom-up in span-major order, one round of the
+ * encode grid per launch and at most one span row (cols / 16 tiles) per
+ * launch; each launch's errors are fed back before the next one starts.
  */
 EXL3_API size_t exl3_ldlq_workspace_bytes(int64_t rows, int64_t cols, int K);
 EXL3_API exl3_status exl3_ldlq(const float *R, int64_t rows, int64_t cols, const float *M, int K,

@@ -582,6 +582,29 @@ def test_ldlq_small_workspace_and_no_q(ex):
     assert np.array_equal(res["codes"].cpu().numpy().view(np.uint16), ref["codes"])
 
 
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_ldlq_launches_straddle_span_rows(ex, K):
+    """A workspace of five encode blocks on a 16-tile-wide matrix: each launch codes
+    5 tiles (K >= 3: 10, a pair per block), so launches start in the middle of a span
+    row and cover the end of one row and the start of the next, and the target and
+    code rings wrap; codes and Q bit-exact against the oracle."""
+    from oracle import ldlq as OL
+    n, cols = 128, 256
+    H = inputs.spd_hessian(n, 60 + K, rho=0.95)
+    Mo, _, _ = OL.block_ldl(H.numpy())
+    R = inputs.iid_f32(n, cols, 70 + K)
+    s = float(np.float32(oracle.rms(R.numpy())))
+    M, _ = ex.block_ldl(H.to(DEV))
+    emin = ex.encode_workspace_min_bytes(K)
+    fixed = ex.ldlq_workspace_bytes(n, cols, K) - 16 * emin
+    ws = torch.empty(fixed + 5 * emin, dtype=torch.uint8, device=DEV)
+    res = ex.ldlq(R.to(DEV), M, K, s, ws=ws)
+    torch.cuda.synchronize()
+    ref = OL.ldlq(R.numpy(), Mo, K, s)
+    assert np.array_equal(res["codes"].cpu().numpy().view(np.uint16), ref["codes"])
+    assert np.array_equal(res["Q"].cpu().numpy(), ref["Q"])
+
+
 def test_ldlq_full_size_properties(ex):
     """4096 x 4096 K=2 with a 4096-channel synthetic Hessian: the factor is
     bit-exact against the oracle's (all 16.8 M entries) and block-diagonalises
