@@ -722,6 +722,58 @@ __device__ __forceinline__ void tb2_advance(Tb2 &tb, uint32_t *bs) {
         tb.on = false;
 }
 
+// The pair kernel's streamed traceback at K = 3 (see tb_drain_streamed): warps 0
+// and 1 each stream the packed rows of their own tile, kTb2Ahead<K> rows ahead.
+template <int K>
+constexpr int kTb2Ahead = K == 3 ? 12 : 16;
+template <int K>
+constexpr size_t kTb2StreamBytes = (size_t)2 * kTb2Ahead<K> * Dual<K>::RW * sizeof(uint32_t);
+
+template <int K>
+__device__ __forceinline__ void tb2_copy_row(uint32_t *dst, const uint32_t *src, const int lane) {
+#pragma unroll
+    for (int i = 0; i < Dual<K>::RW / 128; i++) {     // RW / 4 chunks of 16 bytes
+        const int c = (lane + 32 * i) * 4;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                     ::"r"((uint32_t)__cvta_generic_to_shared(dst + c)), "l"(src + c) : "memory");
+    }
+}
+
+template <int K>
+__device__ __noinline__ Tb2 tb2_drain_streamed(Tb2 tb, uint32_t *bs, uint32_t *pf, const int lane) {
+    constexpr int RW = Dual<K>::RW, A = kTb2Ahead<K>;
+    const unsigned long long rp = __shfl_sync(0xffffffffu, (unsigned long long)(uintptr_t)tb.rows, 0);
+    const int t0 = __shfl_sync(0xffffffffu, tb.t, 0);
+    const int n = t0 - __shfl_sync(0xffffffffu, tb.stop, 0);
+    const int row0 = __shfl_sync(0xffffffffu, tb.row0, 0);
+    const uint32_t *first = reinterpret_cast<const uint32_t *>((uintptr_t)rp) + (size_t)(t0 - 1 - row0) * RW;
+#pragma unroll 1
+    for (int q = 0; q < A; q++) {
+        if (q < n)
+            tb2_copy_row<K>(pf + q * RW, first - (size_t)q * RW, lane);
+        cp_async_commit();
+    }
+#pragma unroll 1
+    for (int q = 0; q < n; q++) {
+        cp_async_wait<A - 1>();
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t off = Dual<K>::bit_of(tb.s >> K);
+            const uint32_t *r = pf + (q % A) * RW + (off >> 5);
+            const uint32_t hi = (K == 3 && (off & 31u) > 29u) ? r[1] : 0u;
+            tb.pending = (unsigned long long)r[0] | ((unsigned long long)hi << 32);
+            tb2_advance<K>(tb, bs);
+        }
+        __syncwarp();
+        if (q + A < n)
+            tb2_copy_row<K>(pf + (q % A) * RW, first - (size_t)(q + A) * RW, lane);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    return tb;
+}
+
 template <int K, int TT>
 __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch a) {
     using Gm = Geo<K>;
@@ -731,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
     float *ysb = Mb + 4 * Gm::G;                                   // [x][256]
     uint32_t *bsb = reinterpret_cast<uint32_t *>(ysb + 512);       // [x][32]
     unsigned long long *red = reinterpret_cast<unsigned long long *>(bsb + 64);   // [32]
+    uint32_t *pf = reinterpret_cast<uint32_t *>(red + 32);        // [warp][kTb2Ahead][RW]
     __shared__ uint32_t sh_sstar[2][2], sh_end[2][2];             // [unit slot][x]
     // this thread's traceback (threads 0 and 32 only): registers at K = 4 (1.7 %
     // faster), shared memory at K = 3 (2.5 % slower in registers)
@@ -919,6 +972,18 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
                 a.tile_cost[tile_at(a, 2 * f_loc + x, grid)] = __fadd_rn(M1x[e >> K], __fmul_rn(d, d));
             }
         }
+        if constexpr (K == 3) {
+            // no forward pass beside the tracebacks: warps 0 and 1 stream their rows
+            // (at K = 4 the call site alone cost the forward loop 1.3 %, so K = 4
+            // keeps the load chain)
+            if (b_loc >= 0 && !fwd && (tid < 32 || (tid < 64 && has_b1))) {
+                const int w = tid >> 5;
+                const Tb2 r = tb2_drain_streamed<K>(tbs[w], bsb + 32 * w,
+                                                    pf + (size_t)w * kTb2Ahead<K> * Du::RW, tid & 31);
+                if ((tid & 31) == 0)
+                    tbs[w] = r;
+            }
+        }
         if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
             Tb2 &tb = K == 4 ? tb_local : tbs[my_tb & 1];
             uint32_t *bs = bsb + 32 * my_tb;
@@ -941,7 +1006,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
 template <int K, int TT>
 exl3_status launch_dual(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
-    const size_t smem = (size_t)(4 * Gm::G + 512 + 64) * sizeof(float) + 32 * sizeof(unsigned long long);
+    const size_t smem = (size_t)(4 * Gm::G + 512 + 64) * sizeof(float) + 32 * sizeof(unsigned long long) +
+                        (K == 3 ? kTb2StreamBytes<K> : 0);
     cudaError_t e = cudaFuncSetAttribute(encode2_kernel<K, TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
