@@ -19,6 +19,9 @@
 //   Feedback, binary32: after span j is coded, every row r above it gets
 //     acc[r][c] = fmaf(M[i][r], E[i][c], acc[r][c]) for i = 16j+15 down to 16j,
 //     E = fl32(R - Q); span b is coded from U = fl32(R + acc).
+// Since column c's accumulators take only column c's errors, the feedback is
+// applied per tile (16 columns) as soon as a tile is coded, with the same
+// per-accumulator order; see run_ldlq for the launch schedule.
 #include "common.cuh"
 
 namespace exl3 {
