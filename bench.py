@@ -63,10 +63,10 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu + encode_common.cuh + common.cuh -> DRAM bytes (read +
     # write) per tile at K=2, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
-    # on 1,216 tiles of N(0, 1) targets (bench.py --case encode --K 2 --rows 1216
-    # --cols 256): 31.93 MB + 1.8495 GB; the traffic is the decision rows,
-    # proportional to the tiles processed.
-    "0bd58932d6ed4d4a1aef03b75456eb46ddb8798e41e4bf7a77a9743ff4bd190a": 1547240.0,
+    # on one full 4096x4096 launch (bench.py --case encode --K 2 --rows 4096 --cols
+    # 4096 --reps 1; one pass): 1.79 GB + 102.77 GB over 65,536 tiles, the bench's
+    # own launch shape.  The writes are the decision rows (383 x 4 KiB per tile).
+    "1538359df9e9910ee57768888c38421624782620f79a2a0a68e3a666b27fe9b6": 1595459.0,
 }
 
 WORKLOAD = "linear4096_k2"
