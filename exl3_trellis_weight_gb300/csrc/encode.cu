@@ -722,8 +722,8 @@ __device__ __forceinline__ void tb2_advance(Tb2 &tb, uint32_t *bs) {
         tb.on = false;
 }
 
-// The pair kernel's streamed traceback at K = 3 (see tb_drain_streamed): warps 0
-// and 1 each stream the packed rows of their own tile, kTb2Ahead<K> rows ahead.
+// The pair kernel's streamed traceback (see tb_drain_streamed): warps 0 and 1
+// each stream the packed rows of their own tile, kTb2Ahead<K> rows ahead.
 template <int K>
 constexpr int kTb2Ahead = K == 3 ? 12 : 16;
 template <int K>
@@ -774,7 +774,11 @@ __device__ __noinline__ Tb2 tb2_drain_streamed(Tb2 tb, uint32_t *bs, uint32_t *p
     return tb;
 }
 
-template <int K, int TT>
+// ST: launches in which every block codes at most one pair (LDLQ rounds, small
+// matrices), whose tracebacks run with no forward pass beside them, stream their
+// rows (tb2_drain_streamed); other launches take an instantiation without that
+// code (at K = 4 its call site alone cost the forward loop 1.3 %).
+template <int K, int TT, bool ST>
 __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch a) {
     using Gm = Geo<K>;
     using Du = Dual<K>;
@@ -972,16 +976,18 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
                 a.tile_cost[tile_at(a, 2 * f_loc + x, grid)] = __fadd_rn(M1x[e >> K], __fmul_rn(d, d));
             }
         }
-        if constexpr (K == 3) {
+        if constexpr (ST) {
             // no forward pass beside the tracebacks: warps 0 and 1 stream their rows
-            // (at K = 4 the call site alone cost the forward loop 1.3 %, so K = 4
-            // keeps the load chain)
             if (b_loc >= 0 && !fwd && (tid < 32 || (tid < 64 && has_b1))) {
                 const int w = tid >> 5;
-                const Tb2 r = tb2_drain_streamed<K>(tbs[w], bsb + 32 * w,
+                const Tb2 r = tb2_drain_streamed<K>(K == 4 ? tb_local : tbs[w], bsb + 32 * w,
                                                     pf + (size_t)w * kTb2Ahead<K> * Du::RW, tid & 31);
-                if ((tid & 31) == 0)
-                    tbs[w] = r;
+                if ((tid & 31) == 0) {
+                    if (K == 4)
+                        tb_local = r;
+                    else
+                        tbs[w] = r;
+                }
             }
         }
         if (my_tb >= 0 && b_loc >= 0 && (my_tb == 0 || has_b1)) {
@@ -1003,23 +1009,32 @@ __global__ void __launch_bounds__(kThreads, 1) encode2_kernel(const EncodeLaunch
     }
 }
 
-template <int K, int TT>
-exl3_status launch_dual(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+template <int K, int TT, bool ST>
+exl3_status launch_dual_st(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
     using Gm = Geo<K>;
     const size_t smem = (size_t)(4 * Gm::G + 512 + 64) * sizeof(float) + 32 * sizeof(unsigned long long) +
-                        (K == 3 ? kTb2StreamBytes<K> : 0);
-    cudaError_t e = cudaFuncSetAttribute(encode2_kernel<K, TT>,
+                        (ST ? kTb2StreamBytes<K> : 0);
+    cudaError_t e = cudaFuncSetAttribute(encode2_kernel<K, TT, ST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return cuda_check(e, "cudaFuncSetAttribute(encode2)");
     if (profiled)
         profile_encode_begin(s);
-    encode2_kernel<K, TT><<<p.grid, kThreads, smem, s>>>(p);
+    encode2_kernel<K, TT, ST><<<p.grid, kThreads, smem, s>>>(p);
     if (profiled) {
         note_launch();
         profile_encode_end(s);
     }
     return cuda_check(cudaGetLastError(), "encode launch");
+}
+
+template <int K, int TT>
+exl3_status launch_dual(const EncodeLaunch &p, cudaStream_t s, bool profiled) {
+    const int64_t n_tiles = p.row_tiles ? p.rows : (p.rows / 16) * (p.cols / 16);
+    const int64_t work = p.n_work > 0 ? p.n_work : n_tiles;
+    if (work <= 2 * (int64_t)p.grid)          // at most one pair per block
+        return launch_dual_st<K, TT, true>(p, s, profiled);
+    return launch_dual_st<K, TT, false>(p, s, profiled);
 }
 
 template <int K, int TT>
