@@ -32,6 +32,11 @@
 // interval holds the step of both tiles of a pair (6-7 % faster than one tile
 // per interval on 4096 x 4096), with the decision rows packed so that the two
 // pairs in flight use the same per-block workspace slice.
+//
+// A traceback with no forward pass beside it (a block's last tile, launches of
+// one tile or pair per block) reads its rows from shared memory, streamed in
+// ahead by its warp (tb_drain_streamed).  A launch may code a run of tiles
+// from an offset, wrapping over the matrix (tile_at), as LDLQ does.
 #include "encode_common.cuh"
 
 namespace exl3 {
