@@ -64,9 +64,9 @@ ENCODE_TRAFFIC = {
     # sha256 of csrc/encode.cu + encode_common.cuh + common.cuh -> DRAM bytes (read +
     # write) per tile at K=2, from ncu's dram__bytes_read.sum + dram__bytes_write.sum
     # on one full 4096x4096 launch (bench.py --case encode --K 2 --rows 4096 --cols
-    # 4096 --reps 1; one pass): 1.79 GB + 102.77 GB over 65,536 tiles, the bench's
+    # 4096 --reps 1; one pass): 1.81 GB + 102.77 GB over 65,536 tiles, the bench's
     # own launch shape.  The writes are the decision rows (383 x 4 KiB per tile).
-    "1538359df9e9910ee57768888c38421624782620f79a2a0a68e3a666b27fe9b6": 1595459.0,
+    "c551039976fce7fbabf72ded171fb8894dddfde45745462e1b22d1faa7d4b71d": 1595764.0,
 }
 
 WORKLOAD = "linear4096_k2"
