@@ -4,23 +4,24 @@
 // butterflies then one exact 2^-7).
 //
 // Same arithmetic and stage order as rotate_fwd.cu (bit-identical results);
-// what differs is the data movement.  One persistent 512-thread block per SM
-// walks the 128 x 128 blocks blockIdx.x, + gridDim.x, ...:
+// what differs is the data movement.  Persistent 128-thread blocks, two per SM,
+// walk the 128 x 128 blocks blockIdx.x, + gridDim.x, ...:
 //   - the bf16 block arrives by two TMA loads (64-column boxes, 128-byte
-//     swizzle) into one of two input stages, with its 128 column signs sv and
-//     128 row signs su (two 512-byte bulk copies on the same transaction
-//     barrier); the loads of the next block are issued before the current one
-//     is transformed, so they overlap the work;
-//   - the fp32 result is written to an output stage in shared memory and
-//     leaves by one TMA store (128 x 128 box) that overlaps the next block;
-//   - between the three butterfly phases the block is exchanged through a
-//     transpose buffer whose 16-byte groups are XOR-swizzled by the row
-//     (offset function tr_off), so every phase's shared accesses are
-//     conflict-free.
-// Phase 1 takes 8 rows per group of 8 lanes (lane bits 0-2 = row, 3-4 = column
-// quarter), so its 16-byte reads of the swizzled input stage hit 8 distinct
-// bank groups.  Shared memory: 2 x 33 KiB input stages, 64 KiB transpose
-// buffer, 64 KiB output stage.
+//     swizzle) into the input stage, with its 128 column signs sv and 128 row
+//     signs su (two 512-byte bulk copies on the same transaction barrier); the
+//     next block's load is issued as soon as every thread has read the stage;
+//   - phase A: thread t holds row t (128 values in registers): the column signs,
+//     all seven column spans, the row sign; the rows go to a transpose buffer
+//     whose element (j, r) sits at j * 128 + (r ^ 4 (j & 7)), so the scalar
+//     writes (one j, 32 consecutive r per warp) and the 16-byte reads of phase B
+//     (4 consecutive r of 32 consecutive j) are conflict-free;
+//   - phase B: thread t holds column t: all seven row spans and the 2^-7 scale;
+//     the result is written row-major over the same buffer (after every column
+//     has been read) and leaves by one 128 x 128 TMA store, which overlaps the
+//     next block until the next transpose write.
+// Two arrangements instead of three move about 288 KiB of shared memory per
+// block instead of 416 KiB (4096 x 4096: 22.45 -> 20.95 us).  Shared memory:
+// a 33 KiB input stage and a 64 KiB transpose/output buffer.
 //
 // Each wait for a TMA load is bounded in time: on expiry the block stops
 // waiting, issues no further load, waits (bounded) for the loads it issued,
@@ -42,13 +43,12 @@ namespace exl3 {
 
 namespace {
 
-constexpr int kTmaThreads = 512;
+constexpr int kTmaThreads = 128;                        // one row, then one column, per thread
 constexpr uint32_t kBlockBytes = 128 * 128 * 2;        // one bf16 block (two 16 KiB boxes)
 constexpr uint32_t kSignBytes = 2 * 128 * 4;           // sv[c0 .. c0+127], su[r0 .. r0+127]
-constexpr uint32_t kStageBytes = kBlockBytes + 1024;   // keeps every stage 1024-byte aligned
-constexpr uint32_t kTOff = 2 * kStageBytes;            // transpose buffer
-constexpr uint32_t kOOff = kTOff + 128 * 128 * 4;      // output stage
-constexpr uint32_t kSmemBytes = kOOff + 128 * 128 * 4; // 194 KiB
+constexpr uint32_t kStageBytes = kBlockBytes + 1024;   // keeps the transpose buffer 1024-byte aligned
+constexpr uint32_t kTOff = kStageBytes;                // transpose buffer, then the output stage
+constexpr uint32_t kSmemBytes = kTOff + 128 * 128 * 4; // 97 KiB: two blocks per SM
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 __device__ unsigned int g_rot_wait_timeouts;
@@ -57,21 +57,51 @@ __device__ __forceinline__ uint32_t saddr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// transpose buffer: row i (128 floats), 16-byte group g = j >> 2 stored at g ^ (i & 7)
-__device__ __forceinline__ int tr_off(int i, int j) {
-    return i * 128 + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3);
+// transpose buffer: element (j, r) -- column j of the rotated rows, row r -- at
+// j * 128 + (r ^ 4 (j & 7)): a warp writing one j for 32 consecutive r and a warp
+// reading 4 consecutive r of 32 consecutive j (16 bytes each) are both conflict-free
+__device__ __forceinline__ int tr_off(int j, int r) {
+    return j * 128 + (r ^ ((j & 7) << 2));
 }
 
+__device__ __forceinline__ void bfly_pair(float &a0, float &a1, float &b0, float &b1) {
+    asm("{\n\t.reg .b64 a, b, s, d;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 s, a, b;\n\t"
+        "sub.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, s;\n\t"
+        "mov.b64 {%2, %3}, d;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
+// one butterfly stage of span SPAN over all N elements (unnormalised)
 template <int SPAN, int N>
 __device__ __forceinline__ void bfly(float (&x)[N]) {
+    if constexpr (SPAN == 1) {
 #pragma unroll
-    for (int e = 0; e < N; e++) {
-        if ((e & SPAN) == 0) {
-            const float a = x[e], b = x[e + SPAN];
+        for (int e = 0; e < N; e += 2) {
+            const float a = x[e], b = x[e + 1];
             x[e] = __fadd_rn(a, b);
-            x[e + SPAN] = __fsub_rn(a, b);
+            x[e + 1] = __fsub_rn(a, b);
         }
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; e += 2)
+            if ((e & SPAN) == 0)
+                bfly_pair(x[e], x[e + 1], x[e + SPAN], x[e + SPAN + 1]);
     }
+}
+
+template <int N>
+__device__ __forceinline__ void fwht(float (&x)[N]) {
+    bfly<1>(x);
+    bfly<2>(x);
+    bfly<4>(x);
+    bfly<8>(x);
+    bfly<16>(x);
+    bfly<32>(x);
+    bfly<64>(x);
 }
 
 __device__ __forceinline__ bool bar_test(uint32_t a, uint32_t parity) {
@@ -124,156 +154,111 @@ __device__ __forceinline__ void issue_load(const CUtensorMap *map, const float *
                  :: "r"(stage_addr + kBlockBytes + 512u), "l"((uint64_t)(su + r0)), "r"(bar) : "memory");
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaThreads, 2)
     rotate_fwd_tma_kernel(const __grid_constant__ CUtensorMap in_map,
                           const __grid_constant__ CUtensorMap out_map, const float *__restrict__ su,
                           const float *__restrict__ sv, const int rows, const int cols,
                           double *tile_sums) {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) unsigned long long full[2];
+    __shared__ __align__(8) unsigned long long full;
     __shared__ int gave_up;
-    // the swizzled TMA destinations want 1024-byte alignment
+    // the swizzled TMA destination wants 1024-byte alignment
     const uint32_t raw = saddr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *const sb = smem_raw + (base - raw);
     float *const T = reinterpret_cast<float *>(sb + kTOff);
-    float *const O = reinterpret_cast<float *>(sb + kOOff);
     const int t = threadIdx.x;
     const int nbc = cols / 128;
     const int nblk = (rows / 128) * nbc;
-    const uint32_t bar0 = saddr(&full[0]);
+    const uint32_t bar = saddr(&full);
 
     if (t == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar0 + 8u) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         gave_up = 0;
     }
     __syncthreads();
-    // loads issued per input stage (thread 0's count; every load is waited on
-    // before the next one on the same stage is issued, so at most one is in
-    // flight per stage and each barrier is at most one phase behind)
-    int issued0 = 0, issued1 = 0;
+    // loads issued (thread 0's count); each is waited on before the next is issued,
+    // so the barrier is at most one phase behind
+    int issued = 0;
     // programmatic dependent launch: everything above overlaps the previous
     // kernel's tail; global memory is read only after it has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (t == 0 && (int)blockIdx.x < nblk) {
-        issue_load(&in_map, su, sv, base, bar0, (int)blockIdx.x, nbc);
-        issued0 = 1;
+        issue_load(&in_map, su, sv, base, bar, (int)blockIdx.x, nbc);
+        issued = 1;
     }
 
     int it = 0;
     for (int blk = (int)blockIdx.x; blk < nblk; blk += (int)gridDim.x, it++) {
-        const int st = it & 1;
         const int r0 = (blk / nbc) * 128, c0 = (blk % nbc) * 128;
-        // the other stage was last read in the previous block's phase 1 and its
-        // load was waited on there; after a wait gave up no load is issued any
-        // more (a second arrival on a barrier phase still in flight is not allowed)
-        if (t == 0 && blk + (int)gridDim.x < nblk && !gave_up) {
-            issue_load(&in_map, su, sv, base + (uint32_t)(st ^ 1) * kStageBytes,
-                       bar0 + 8u * (uint32_t)(st ^ 1), blk + (int)gridDim.x, nbc);
-            if (st)
-                issued0++;
-            else
-                issued1++;
-        }
-        bar_wait(bar0 + 8u * (uint32_t)st, (uint32_t)(it >> 1) & 1u, &gave_up);
-        // the last block of this CTA: the next kernel in the stream may start its prologue
+        bar_wait(bar, (uint32_t)it & 1u, &gave_up);
         if (blk + (int)gridDim.x >= nblk)
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-        // ---- phase 1: row i, columns 32 jh .. 32 jh + 31 -> j spans 1..16 -------
+        // ---- phase A: row t, every column span (1 .. 64), then the row sign ----
+        float x[128];
+        float s_row;
         {
-            const int i = (t & 7) + 8 * (t >> 5), jh = (t >> 3) & 3;
-            const unsigned char *stage = sb + (uint32_t)st * kStageBytes;
-            const unsigned char *row = stage + (jh >> 1) * (kBlockBytes / 2) + i * 128;
-            const float4 *svp = reinterpret_cast<const float4 *>(stage + kBlockBytes) + 8 * jh;
-            float x[32];
+            const float4 *svp = reinterpret_cast<const float4 *>(sb + kBlockBytes);
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                // 16-byte group (jh & 1) * 4 + q of the 128-byte box row, swizzled by the row
-                const int g = ((jh & 1) * 4 + q) ^ (i & 7);
-                const uint4 w = *reinterpret_cast<const uint4 *>(row + 16 * g);
-                const float4 s0 = svp[2 * q], s1 = svp[2 * q + 1];
-                x[8 * q + 0] = __fmul_rn(__uint_as_float(w.x << 16), s0.x);
-                x[8 * q + 1] = __fmul_rn(__uint_as_float(w.x & 0xFFFF0000u), s0.y);
-                x[8 * q + 2] = __fmul_rn(__uint_as_float(w.y << 16), s0.z);
-                x[8 * q + 3] = __fmul_rn(__uint_as_float(w.y & 0xFFFF0000u), s0.w);
-                x[8 * q + 4] = __fmul_rn(__uint_as_float(w.z << 16), s1.x);
-                x[8 * q + 5] = __fmul_rn(__uint_as_float(w.z & 0xFFFF0000u), s1.y);
-                x[8 * q + 6] = __fmul_rn(__uint_as_float(w.w << 16), s1.z);
-                x[8 * q + 7] = __fmul_rn(__uint_as_float(w.w & 0xFFFF0000u), s1.w);
-            }
-            bfly<1>(x);
-            bfly<2>(x);
-            bfly<4>(x);
-            bfly<8>(x);
-            bfly<16>(x);
+            for (int h = 0; h < 2; h++)
 #pragma unroll
-            for (int q = 0; q < 8; q++)
-                *reinterpret_cast<float4 *>(T + tr_off(i, 32 * jh + 4 * q)) =
-                    make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                for (int g = 0; g < 8; g++) {
+                    // 16-byte group g of the 128-byte row of box h, swizzled by the row
+                    const uint4 w = *reinterpret_cast<const uint4 *>(sb + h * (kBlockBytes / 2) + t * 128 +
+                                                                     ((g ^ (t & 7)) << 4));
+                    const int j = 64 * h + 8 * g;
+                    const float4 s0 = svp[j / 4], s1 = svp[j / 4 + 1];
+                    x[j + 0] = __fmul_rn(__uint_as_float(w.x << 16), s0.x);
+                    x[j + 1] = __fmul_rn(__uint_as_float(w.x & 0xFFFF0000u), s0.y);
+                    x[j + 2] = __fmul_rn(__uint_as_float(w.y << 16), s0.z);
+                    x[j + 3] = __fmul_rn(__uint_as_float(w.y & 0xFFFF0000u), s0.w);
+                    x[j + 4] = __fmul_rn(__uint_as_float(w.z << 16), s1.x);
+                    x[j + 5] = __fmul_rn(__uint_as_float(w.z & 0xFFFF0000u), s1.y);
+                    x[j + 6] = __fmul_rn(__uint_as_float(w.w << 16), s1.z);
+                    x[j + 7] = __fmul_rn(__uint_as_float(w.w & 0xFFFF0000u), s1.w);
+                }
+            s_row = reinterpret_cast<const float *>(sb + kBlockBytes + 512u)[t];
         }
-        __syncthreads();
-
-        // ---- phase 2: rows 8 ib .. 8 ib + 7, columns jlo + 32 jh ----------------
-        {
-            const int ib = t >> 5, jlo = t & 31;
-            const float *sus = reinterpret_cast<const float *>(sb + (uint32_t)st * kStageBytes + kBlockBytes + 512u);
-            float x[32];                               // x[8 jh + il]
-#pragma unroll
-            for (int jh = 0; jh < 4; jh++)
-#pragma unroll
-                for (int il = 0; il < 8; il++)
-                    x[8 * jh + il] = T[tr_off(8 * ib + il, jlo + 32 * jh)];
-            bfly<8>(x);                                // j span 32
-            bfly<16>(x);                               // j span 64
-#pragma unroll
-            for (int il = 0; il < 8; il++) {
-                const float s = sus[8 * ib + il];
-#pragma unroll
-                for (int jh = 0; jh < 4; jh++)
-                    x[8 * jh + il] = __fmul_rn(x[8 * jh + il], s);
-            }
-            bfly<1>(x);                                // i span 1
-            bfly<2>(x);                                // i span 2
-            bfly<4>(x);                                // i span 4
-#pragma unroll
-            for (int jh = 0; jh < 4; jh++)
-#pragma unroll
-                for (int il = 0; il < 8; il++)
-                    T[tr_off(8 * ib + il, jlo + 32 * jh)] = x[8 * jh + il];
+        __syncthreads();                 // the input stage is free: load the next block
+        if (t == 0 && blk + (int)gridDim.x < nblk && !gave_up) {
+            issue_load(&in_map, su, sv, base, bar, blk + (int)gridDim.x, nbc);
+            issued++;
         }
-        // the previous block's store must have finished reading the output stage
+        fwht(x);
+#pragma unroll
+        for (int j = 0; j < 128; j++)
+            x[j] = __fmul_rn(x[j], s_row);
+        // the previous block's store must have finished reading the buffer
         if (t == 0)
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 128; j++)
+            T[tr_off(j, t)] = x[j];
+        __syncthreads();
 
-        // ---- phase 3: rows ilo + 8 ih, columns 2 jp, 2 jp + 1 -> i spans 8..64 ---
-        {
-            const int ilo = t >> 6, jp = t & 63;
-            float x[32];                               // x[2 ih + jb]
+        // ---- phase B: column t, every row span (1 .. 64), then 2^-7 ----
 #pragma unroll
-            for (int ih = 0; ih < 16; ih++) {
-                const float2 v = *reinterpret_cast<const float2 *>(T + tr_off(ilo + 8 * ih, 2 * jp));
-                x[2 * ih] = v.x;
-                x[2 * ih + 1] = v.y;
-            }
-            bfly<2>(x);                                // i span 8
-            bfly<4>(x);                                // i span 16
-            bfly<8>(x);                                // i span 32
-            bfly<16>(x);                               // i span 64
-#pragma unroll
-            for (int ih = 0; ih < 16; ih++)
-                *reinterpret_cast<float2 *>(O + (ilo + 8 * ih) * 128 + 2 * jp) =
-                    make_float2(__fmul_rn(x[2 * ih], 0x1p-7f), __fmul_rn(x[2 * ih + 1], 0x1p-7f));
+        for (int q = 0; q < 32; q++) {
+            const float4 v = *reinterpret_cast<const float4 *>(T + t * 128 + ((q ^ (t & 7)) << 2));
+            x[4 * q] = v.x;
+            x[4 * q + 1] = v.y;
+            x[4 * q + 2] = v.z;
+            x[4 * q + 3] = v.w;
         }
+        __syncthreads();                 // every column is read: the buffer takes the output
+        fwht(x);
+#pragma unroll
+        for (int i = 0; i < 128; i++)
+            T[i * 128 + t] = __fmul_rn(x[i], 0x1p-7f);
         // generic-proxy writes of the output stage, then one TMA store of it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (t == 0) {
             asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
-                         :: "l"((uint64_t)&out_map), "r"(c0), "r"(r0), "r"(base + kOOff)
+                         :: "l"((uint64_t)&out_map), "r"(c0), "r"(r0), "r"(base + kTOff)
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
@@ -283,29 +268,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             double s = 0.0;
             for (int i = 0; i < 16; i++)
                 for (int j = 0; j < 16; j++) {
-                    const double v = (double)O[(ti * 16 + i) * 128 + tj * 16 + j];
+                    const double v = (double)T[(ti * 16 + i) * 128 + tj * 16 + j];
                     s = __dadd_rn(s, __dmul_rn(v, v));
                 }
             tile_sums[(size_t)((r0 >> 4) + ti) * (size_t)(cols / 16) + (c0 >> 4) + tj] = s;
         }
     }
     if (t == 0) {
-        // after a wait gave up, the last load of each stage may still be in
-        // flight: wait (bounded) for it before the block exits, so that no copy
-        // lands in shared memory of a block that is gone.  Stage s has completed
-        // phases 0 .. n - 1 (n loads issued on it) once that load has landed.
-        if (gave_up) {
-            for (int s = 0; s < 2; s++) {
-                const int n = s ? issued1 : issued0;
-                if (n == 0)
-                    continue;
-                const uint32_t parity = (uint32_t)(n - 1) & 1u;
-                unsigned long long t0, t1;
-                asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
-                do {
-                    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
-                } while (!bar_test(bar0 + 8u * (uint32_t)s, parity) && t1 - t0 < kWaitLimitNs);
-            }
+        // after a wait gave up, the last load issued may still be in flight: wait
+        // (bounded) for it before the block exits, so that no copy lands in shared
+        // memory of a block that is gone (n loads issued: phase n - 1 completes it)
+        if (gave_up && issued > 0) {
+            const uint32_t parity = (uint32_t)(issued - 1) & 1u;
+            unsigned long long t0, t1;
+            asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
+            do {
+                asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
+            } while (!bar_test(bar, parity) && t1 - t0 < kWaitLimitNs);
         }
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
@@ -373,7 +352,8 @@ exl3_status launch_rotate_fwd_tma(const RotateLaunch &p, cudaStream_t s) {
                                          (int)smem);
     if (e != cudaSuccess)
         return cuda_check(e, "cudaFuncSetAttribute(rotate_fwd_tma)");
-    const int64_t grid = nblk < device_sm_count() ? nblk : device_sm_count();
+    const int64_t slots = 2 * (int64_t)device_sm_count();     // two blocks per SM
+    const int64_t grid = nblk < slots ? nblk : slots;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kTmaThreads);
