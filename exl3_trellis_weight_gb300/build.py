@@ -6,6 +6,7 @@ separately rounded IEEE operation (no FMA contraction).
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -48,6 +49,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # processes that build at once (ranks of one job) take turns; a later one
+    # finds the library fresh and returns
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale():
+            return LIB
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose: bool) -> str:
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose else []
 
